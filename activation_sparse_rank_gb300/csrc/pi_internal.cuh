@@ -1,0 +1,164 @@
+// Internal declarations shared by the translation units of libpi.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "pi.h"
+
+// Device status bits (set with atomicOr, read and cleared by pi_device_status).
+#define PI_STATUS_BAD_INDEX 1u
+#define PI_STATUS_BAD_COUNT 2u
+
+struct pi_layer {
+  int d = 0, ffn = 0, rank = 0, act = 0;
+  int device = 0, num_sms = 0;
+  char *base = nullptr;          // one device allocation holding everything below
+  size_t bytes = 0;
+  __half *W_p1 = nullptr;        // [rank, d]
+  __half *W_p2 = nullptr;        // [ffn, rank]   permuted rows
+  __half *W_up = nullptr;        // [ffn, d]      permuted rows
+  __half *W_gate = nullptr;      // [ffn, d]      permuted rows (ReGLU)
+  __half *W_dT = nullptr;        // [ffn, d]      W_down^T, permuted rows
+  float *b = nullptr;            // [ffn]         permuted
+  float *c_p = nullptr;          // [ffn]         permuted (zeros when absent)
+  unsigned int *status = nullptr;
+  std::vector<int32_t> perm;     // host copy of the permutation
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;   // profiling hook
+};
+
+namespace pi {
+
+// ---- errors ---------------------------------------------------------------
+pi_status fail(pi_status s, const char *fmt, ...);
+pi_status cuda_fail(cudaError_t e, const char *what);
+
+#define PI_TRY_CUDA(call)                                     \
+  do {                                                        \
+    cudaError_t e_ = (call);                                  \
+    if (e_ != cudaSuccess) return pi::cuda_fail(e_, #call);   \
+  } while (0)
+
+// ---- workspace --------------------------------------------------------------
+// Layout of the caller's workspace for batches of up to B tokens.
+struct WsLayout {
+  size_t h = 0;        // float [B, rank]
+  size_t a = 0;        // float [B, ffn]        activations by list position
+  size_t partial = 0;  // float [nsplit, B, d]  split-K partial sums
+  size_t mask = 0;     // uint8 [B, ffn]
+  size_t idx = 0;      // int32 [ffn]           (pi_layer_forward when idx not given)
+  size_t count = 0;    // int32 [4]
+  size_t total = 0;
+};
+WsLayout ws_layout(const pi_layer *L, int B);
+int fused_splits(const pi_layer *L);        // CTAs of the batch-1 fused kernel
+int down_splits(const pi_layer *L, int B);  // split count of the generic down kernel
+int down_colblocks(const pi_layer *L);      // column blocks of the generic down kernel
+
+// ---- launch helpers ---------------------------------------------------------
+// Launch with programmatic dependent launch (the kernel must execute
+// griddepcontrol.wait before touching anything a predecessor writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Record the layer's profiling event (if set) on s; external record when capturing.
+cudaError_t record_hook(cudaEvent_t ev, cudaStream_t s);
+
+// Stage launchers (pi_predict.cu / pi_sparse.cu).  All asynchronous.
+cudaError_t run_predict(const pi_layer *L, const __half *x, int B, uint8_t *mask,
+                        float *logits, float *h_ws, cudaStream_t s);
+cudaError_t run_compact(const pi_layer *L, const uint8_t *mask, int B, int32_t *idx,
+                        int32_t *count, cudaStream_t s);
+// idx == nullptr means the identity list 0..count_const-1 (count ignored).
+cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int32_t *idx,
+                           const int32_t *count, int count_const, float *y,
+                           const WsLayout &w, char *ws, cudaStream_t s);
+cudaError_t run_profile(const pi_layer_desc *desc, const __half *x, int T, int32_t *counts,
+                        cudaStream_t s);
+
+}  // namespace pi
+
+// ---- device helpers ---------------------------------------------------------
+namespace pidev {
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Streaming 16-byte load of weights (read once per use; do not keep in L1).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Ask L2 to fetch `bytes` (multiple of 16, 16-byte aligned) starting at p.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// acc += sum of the 8 products w[e] * x[e]; fp16 products are exact in fp32.
+__device__ __forceinline__ float dot8(float acc, const uint4 &w, const uint4 &x) {
+  const __half2 *wh = reinterpret_cast<const __half2 *>(&w);
+  const __half2 *xh = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float2 wf = __half22float2(wh[e]);
+    float2 xf = __half22float2(xh[e]);
+    acc = fmaf(wf.x, xf.x, acc);
+    acc = fmaf(wf.y, xf.y, acc);
+  }
+  return acc;
+}
+
+// acc[e] += s * w[e] for the 8 halves of w.
+__device__ __forceinline__ void axpy8(float *acc, float s, const uint4 &w) {
+  const __half2 *wh = reinterpret_cast<const __half2 *>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float2 wf = __half22float2(wh[e]);
+    acc[2 * e] = fmaf(s, wf.x, acc[2 * e]);
+    acc[2 * e + 1] = fmaf(s, wf.y, acc[2 * e + 1]);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Read *count once, clamp it to [0, limit] and flag values out of range.
+__device__ __forceinline__ int load_count(const int32_t *count, int count_const, int limit,
+                                          unsigned int *status) {
+  if (count == nullptr) return count_const;
+  int c = *count;
+  if (c < 0 || c > limit) {
+    if (threadIdx.x == 0) atomicOr(status, PI_STATUS_BAD_COUNT);
+    c = c < 0 ? 0 : limit;
+  }
+  return c;
+}
+
+}  // namespace pidev

@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Throughput of the predictor-gated sparse FFN on one GB300 (or N replicas).
+
+Metric: sparse-FFN tokens/s at batch 1, and the effective HBM bandwidth on the
+weight bytes actually touched (predictor + active rows) against peak.
+
+A step is one pass of the whole path over one batch of synthetic input: the
+256 decode tokens of the OPT-7B-shaped stack (d=4096, ffn=16384, r=256,
+32 layers, hot-first neuron order from a 10k-token profile), each token
+through all 32 layers in order (predictor, active list, sparse FFN), batch 1.
+The step is one CUDA graph launch.  Each step streams about 1.2 GB of distinct
+weight rows through a 129 MB L2, so inputs are larger than L2 between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on the host cores instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from workload import config_by_name, make_layer, make_tokens, sub_seed  # noqa: E402
+
+METRIC = "sparse-FFN tokens/s at batch 1; effective HBM GB/s on touched bytes vs peak"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="opt7b_stack")
+    ap.add_argument("--layers", type=int, default=0, help="override layer count (debug)")
+    ap.add_argument("--tokens", type=int, default=0, help="override tokens per step (debug)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def bytes_per_active_neuron(d: int, act: str) -> int:
+    """Weight bytes read per active neuron: its up row (+ gate row) and its
+    W_down^T row, 2d bytes each."""
+    return 2 * d * (3 if act == "reglu" else 2)
+
+
+def predictor_bytes(d: int, ffn: int, r: int) -> int:
+    return 2 * r * d + 2 * ffn * r
+
+
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.err = None
+        gid = self._gpu_id(device_index)
+        cmd = ["nvidia-smi", f"--id={gid}", "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception as e:  # no nvidia-smi
+            self.err = str(e)
+
+    @staticmethod
+    def _gpu_id(i: int) -> str:
+        p = torch.cuda.get_device_properties(i)
+        if all(hasattr(p, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+            return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        if vis:
+            return vis.split(",")[i]
+        return str(i)
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.err or "nvidia-smi unavailable"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"error": "no samples"}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[4:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+def build_stack(cfg, device, n_layers, keep_host_layers):
+    import activation_sparse_rank_gb300 as pi
+    spec = cfg.layer
+    layers, host_layers = [], []
+    for l in range(n_layers):
+        t = make_layer(spec, cfg.seed, l, device=device)
+        perm = None
+        if cfg.profile_tokens:
+            Xp = make_tokens(spec.d, cfg.profile_tokens, sub_seed(cfg.seed, l, "profile"), device)
+            counts = pi.profile_activations(t, Xp)
+            perm = pi.hot_first_perm(counts.cpu().numpy())
+            del Xp
+        layers.append(pi.Layer.from_dict(t, perm=perm))
+        if l < keep_host_layers:
+            host_layers.append({k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                                for k, v in t.items()})
+        del t
+    torch.cuda.synchronize()
+    return layers, host_layers
+
+
+def touched_bytes(cfg, counts: torch.Tensor) -> int:
+    spec = cfg.layer
+    T, L = counts.shape
+    s = int(counts.sum().item())
+    return T * L * predictor_bytes(spec.d, spec.ffn, spec.rank) + s * bytes_per_active_neuron(spec.d, spec.act)
+
+
+def time_oracle(host_layers, X_host, L_total, seconds: float, min_pairs: int = 4):
+    """Float64 oracle on (token, layer) pairs until `seconds` pass; returns
+    tokens/s through an L_total-layer stack and a description of the sample."""
+    from oracle import ffn as O
+    OL = [O.OracleLayer.from_tensors(t) for t in host_layers]
+    pairs = 0
+    t0 = time.perf_counter()
+    tok = 0
+    while True:
+        for li, L in enumerate(OL):
+            O.predicted_forward(L, X_host[tok, li])
+            pairs += 1
+        tok += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and pairs >= min_pairs) or tok >= X_host.shape[0]:
+            break
+    per_pair = el / pairs
+    return 1.0 / (per_pair * L_total), f"{pairs} (token, layer) pairs: tokens 0..{tok - 1} x layers 0..{len(OL) - 1}, {el:.1f} s"
+
+
+def run_reference(args, cfg):
+    """The reference arm: the float64 CPU oracle, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    spec = cfg.layer
+    n_layers = 2
+    host_layers = [{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+                    for k, v in make_layer(spec, cfg.seed, l, device="cpu").items()}
+                   for l in range(n_layers)]
+    T = max(4, args.steps + args.warmup) * 2
+    X = make_tokens(spec.d, T * n_layers, sub_seed(cfg.seed, 0, "bench_x"), "cpu").view(T, n_layers, 1, spec.d)
+    per_step = max(1.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    from oracle import ffn as O
+    OL = [O.OracleLayer.from_tensors(t) for t in host_layers]
+
+    def one_step(tok0):
+        t0 = time.perf_counter()
+        pairs = 0
+        tok = tok0
+        while True:
+            for li, L in enumerate(OL):
+                O.predicted_forward(L, X[tok % T, li])
+                pairs += 1
+            tok += 1
+            if time.perf_counter() - t0 >= per_step:
+                break
+        return time.perf_counter() - t0, pairs, tok
+
+    tok = 0
+    for _ in range(args.warmup):
+        _, _, tok = one_step(tok)
+    tot_t, tot_p = 0.0, 0
+    for _ in range(args.steps):
+        el, p, tok = one_step(tok)
+        tot_t += el
+        tot_p += p
+    value = 1.0 / ((tot_t / tot_p) * cfg.layers)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.description, "name": cfg.name, "d": spec.d, "ffn": spec.ffn,
+                   "rank": spec.rank, "layers": cfg.layers, "batch": 1},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{tot_p} (token, layer) pairs of layers 0..{n_layers - 1}, "
+                                   f"{tot_t:.1f} s, scaled to a {cfg.layers}-layer stack; numpy "
+                                   f"float64 with its default BLAS threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "activation_sparse_rank_gb300" / "csrc").glob("*")):
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def main():
+    args = parse()
+    cfg = config_by_name(args.config)
+    if args.impl == "reference":
+        run_reference(args, cfg)
+        return
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    import activation_sparse_rank_gb300 as pi
+    from activation_sparse_rank_gb300.stack import SparseFFNStack
+
+    spec = cfg.layer
+    n_layers = args.layers or cfg.layers
+    T = args.tokens or cfg.tokens
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
+    t_setup = time.perf_counter()
+    layers, host_layers = build_stack(cfg, device, n_layers, keep_host_layers=2 if want_cpu else 0)
+    stack = SparseFFNStack(layers, tokens=T, B=1)
+    X = make_tokens(spec.d, T * n_layers, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
+    stack.x.copy_(X.view(T, n_layers, 1, spec.d))
+    del X
+    stack.build_graph()
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    s = stack.stream
+    for _ in range(max(3, args.warmup)):
+        with torch.cuda.stream(s):
+            stack.graph.replay()
+    s.synchronize()
+
+    clocks = ClockSampler(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(args.steps):
+            stack.graph.replay()
+    ev1.record(s)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    for layer in layers:
+        if layer.device_status() != 0:
+            raise RuntimeError("device check failed during the timed steps")
+
+    tokens_step = T * 1
+    value = tokens_step * world / (ms / 1000.0)
+    tb = touched_bytes(cfg, stack.count)
+    mean_S = float(stack.count.double().mean().item())
+    eff_gbs = tb / (ms / 1000.0) / 1e9
+    peak, peak_kind = measured_peaks()
+    gpu_launches = stack.launches_per_step() * args.steps
+
+    # dense comparator: the same kernels over every neuron, 16 tokens
+    Td = min(16, T)
+    dense_g = torch.cuda.CUDAGraph()
+    ws = stack.ws
+    yd = torch.empty(n_layers, 1, spec.d, dtype=torch.float32, device=device)
+    with torch.cuda.stream(s):
+        for li, layer in enumerate(layers):
+            layer.dense_ref(stack.x[0, li], yd[li], ws=ws, stream=s)
+    s.synchronize()
+    with torch.cuda.graph(dense_g, stream=s):
+        for t in range(Td):
+            for li, layer in enumerate(layers):
+                layer.dense_ref(stack.x[t, li], yd[li], ws=ws, stream=s)
+    for _ in range(2):
+        dense_g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            dense_g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    dense_tok_s = 3 * Td / (e0.elapsed_time(e1) / 1000.0)
+
+    # dominant kernel (fused up/down) timed inside a captured step
+    Tr = min(32, T)
+    try:
+        evs = {(t, l): (torch.cuda.Event(enable_timing=True, external=True),
+                        torch.cuda.Event(enable_timing=True, external=True))
+               for t in range(Tr) for l in range(n_layers)}
+        for a, b in evs.values():      # materialise the events before capture
+            a.record(s); b.record(s)
+        s.synchronize()
+        save = stack.T
+        stack.T = Tr
+        g_inst = stack.capture(timing_events=evs)
+        stack.T = save
+        with torch.cuda.stream(s):
+            g_inst.replay()
+        s.synchronize()
+        how = "external event-record nodes around each launch inside a captured step"
+    except TypeError:
+        evs = {(t, l): (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for t in range(Tr) for l in range(n_layers)}
+        with torch.cuda.stream(s):
+            for t in range(Tr):
+                for li, layer in enumerate(layers):
+                    layer.set_timing_events(*evs[(t, li)])
+                    layer.forward(stack.x[t, li], stack.idx[li], stack.count[t, li:li + 1],
+                                  stack.y[t, li], ws=ws, stream=s)
+                    layer.set_timing_events(None, None)
+        s.synchronize()
+        how = "events around each launch, eager step"
+    k_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in sorted(evs)]
+    cnt = stack.count[:Tr].cpu().numpy()
+    alg_bytes = float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act)
+    k_avg_ms = sum(k_ms) / len(k_ms)
+    achieved = alg_bytes / len(k_ms) / (k_avg_ms / 1e3) / 1e9
+    traffic = None
+    tfile = ROOT / "profiles" / "fused_traffic.json"
+    if tfile.exists():
+        tj = json.loads(tfile.read_text())
+        if tj.get("kernel_source_hash") == kernel_source_hash():
+            traffic = tj.get("bytes_per_launch")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "k_fused_small (up+down over the active list)",
+                "peak_kind": peak_kind + " (copy bandwidth)",
+                "launches_timed": len(k_ms), "avg_launch_us": k_avg_ms * 1e3,
+                "timing": how}
+
+    # end to end from pinned host buffers through the public API
+    xh = torch.empty_like(stack.x, device="cpu").pin_memory()
+    xh.copy_(stack.x)
+    yh = torch.empty_like(stack.y, device="cpu").pin_memory()
+    for _ in range(2):
+        stack.run_host(xh, yh, stream=s)
+    s.synchronize()
+    E = max(3, min(args.steps, 5))
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(s)
+    for _ in range(E):
+        stack.run_host(xh, yh, stream=s)
+    f1.record(s)
+    s.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / E
+    e2e = {"value": tokens_step * world / (e2e_ms / 1000.0), "unit": "tokens/s",
+           "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+           "d2h_bytes_per_step": yh.numel() * yh.element_size()}
+
+    cpu = None
+    if want_cpu:
+        xh_l = stack.x[:, :2].cpu()
+        v, sample = time_oracle(host_layers, xh_l, n_layers, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": sample + f"; scaled to a {n_layers}-layer stack; numpy float64, default BLAS threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": cfg.description, "name": cfg.name, "d": spec.d,
+                       "ffn": spec.ffn, "rank": spec.rank, "layers": n_layers,
+                       "tokens_per_step": T, "batch": 1, "act": spec.act,
+                       "weights": "fp16", "hot_first": bool(cfg.profile_tokens),
+                       "l2": "inputs larger than L2: ~1.2 GB of distinct weight rows per step",
+                       "parallelism": f"replicas{world}"},
+            "effective_hbm_gbs": eff_gbs,
+            "effective_frac_of_measured": eff_gbs / peak,
+            "effective_frac_of_nominal_8tbs": eff_gbs / (NOMINAL_HBM_GBS),
+            "touched_bytes_per_step": tb, "mean_active": mean_S,
+            "dense_tokens_per_s": dense_tok_s, "speedup_vs_dense": value / world / dense_tok_s,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": gpu_launches, "clocks": clk, "setup_s": setup_s,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

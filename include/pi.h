@@ -1,0 +1,212 @@
+/*
+ * pi.h - C ABI of libpi, the predictor-gated, neuron-aware sparse FFN for
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The method is PowerInfer's decode-time FFN block ("PowerInfer: Fast Large
+ * Language Model Serving with a Consumer-grade GPU", egguo-blog reading
+ * report): per layer an adaptive predictor (section 2.3, core module 3)
+ * selects the neurons expected to fire, and neuron-aware operators (section
+ * 2.3, core module 4) compute only those neurons, directly on the rows of the
+ * weight matrices, with no sparse-format conversion.  The offline profile
+ * (section 2.3, core module 1) becomes a hot-first neuron order of the
+ * resident weight layout.
+ *
+ * Conventions shared by every call:
+ *  - fp16 data is passed as IEEE binary16 bit patterns (uint16_t).
+ *  - "device" pointers are CUDA device (or managed) memory of the current
+ *    device; "host" pointers are ordinary CPU memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call except create/destroy/perm/hot_first_perm/device_status is
+ *    asynchronous on that stream, allocates nothing and copies nothing to
+ *    the host, so a sequence of calls can be captured in a CUDA graph.
+ *  - Active-set sizes never leave the device: `count` is a device int32.
+ *  - Arguments are validated on the host before any launch; a rejected call
+ *    launches nothing.  Device-side checks (an index or count out of range)
+ *    never trap: the offending element is skipped and a status word in the
+ *    layer is set, which pi_device_status() reports.
+ *  - pi_last_error() returns a thread-local message for the last failure.
+ */
+#ifndef PI_H_
+#define PI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PI_OK = 0,
+  PI_ERR_INVALID_ARG = 1,   /* bad pointer, size or shape; nothing launched      */
+  PI_ERR_UNSUPPORTED = 2,   /* shape outside the library's supported range       */
+  PI_ERR_OOM = 3,           /* pi_layer_create could not allocate device memory  */
+  PI_ERR_CUDA = 4,          /* a CUDA runtime call failed (see pi_last_error)    */
+  PI_ERR_DEVICE_CHECK = 5   /* a kernel found an out-of-range index or count     */
+} pi_status;
+
+typedef enum {
+  PI_ACT_RELU = 0,   /* a_i = max(0, W_up_i.x + b_i)                           */
+  PI_ACT_REGLU = 1   /* a_i = max(0, W_gate_i.x + b_i) * (W_up_i.x)            */
+} pi_act;
+
+/* Shape limits (PI_ERR_UNSUPPORTED outside them). */
+#define PI_MAX_D      16384   /* d % 8 == 0 */
+#define PI_MAX_RANK   2048    /* rank % 8 == 0 */
+#define PI_MAX_FFN    (1 << 20)
+#define PI_MAX_BATCH  128
+
+typedef struct pi_layer pi_layer;
+
+/* One FFN layer in model space, PyTorch nn.Linear weight layouts, all device
+ * pointers.  Read only during pi_layer_create / pi_profile_activations.
+ *   W_up   [ffn, d]   fp16  up projection
+ *   W_gate [ffn, d]   fp16  gate projection (PI_ACT_REGLU only, else NULL)
+ *   b      [ffn]      fp32  bias of the gated projection (up for ReLU, gate for ReGLU)
+ *   W_down [d, ffn]   fp16  down projection
+ *   W_p1   [rank, d]  fp16  predictor first layer (no bias)
+ *   W_p2   [ffn, rank] fp16 predictor second layer
+ *   c_p    [ffn]      fp32  predictor output bias, or NULL for zero */
+typedef struct {
+  int32_t d, ffn, rank;
+  int32_t act;               /* pi_act */
+  const uint16_t *W_up;
+  const uint16_t *W_gate;
+  const float *b;
+  const uint16_t *W_down;
+  const uint16_t *W_p1;
+  const uint16_t *W_p2;
+  const float *c_p;
+} pi_layer_desc;
+
+/* Build a layer object that owns a permuted, neuron-major copy of the weights
+ * (section 2.3, core module 1 and variable table: neurons ordered by profiled
+ * activation frequency v_i = f_i, hot first).
+ *   perm  host int32 [ffn] or NULL (identity): position k of the layer holds
+ *         model neuron perm[k]; must be a permutation of 0..ffn-1.
+ * The library copies W_p1 as is, permutes the rows of W_up, W_gate, b, W_p2,
+ * c_p, and stores W_down transposed and permuted as W_down^T [ffn, d] so that
+ * each neuron's down weights are one contiguous row.  Peak device memory is
+ * the caller's weights plus one layer copy.  Synchronous: returns after the
+ * copy finished on `stream`.  The caller may free its buffers afterwards.
+ * Errors: PI_ERR_INVALID_ARG (NULL pointer, bad perm), PI_ERR_UNSUPPORTED
+ * (shape), PI_ERR_OOM, PI_ERR_CUDA. *out is NULL on failure. */
+pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *desc,
+                          const int32_t *perm, void *stream);
+
+/* Free the layer and its device memory (synchronizes the device first).
+ * NULL is accepted. */
+pi_status pi_layer_destroy(pi_layer *layer);
+
+/* Shape of a layer (any output pointer may be NULL). */
+pi_status pi_layer_info(const pi_layer *layer, int32_t *d, int32_t *ffn,
+                        int32_t *rank, int32_t *act);
+
+/* Copy the layer's permutation (host int32 [ffn]): position k holds model
+ * neuron perm[k].  Active-set indices returned by this library are positions
+ * k, i.e. in permuted space. */
+pi_status pi_layer_perm(const pi_layer *layer, int32_t *perm);
+
+/* Bytes of device workspace that pi_predict, pi_sparse_ffn, pi_ffn_dense_ref
+ * and pi_layer_forward need for batches of up to B_max tokens (0 on bad
+ * arguments).  The workspace is caller-owned scratch; calls that run
+ * concurrently need separate workspaces. */
+size_t pi_workspace_bytes(const pi_layer *layer, int32_t B_max);
+
+/* Adaptive predictor (section 2.3, core module 3): for each token b < B,
+ *   h = max(0, W_p1 x_b)            binary32 accumulation, h kept in binary32
+ *   l = W_p2 h + c_p                binary32
+ *   mask[b, i] = (l_i > 0)          i.e. sigmoid(l_i) > 0.5; l_i == 0 is inactive
+ *   x       device fp16 [B, d] (model space; rows contiguous)
+ *   mask    device uint8 [B, ffn] (permuted space), values 0/1, or NULL
+ *   logits  device fp32 [B, ffn] (permuted space), or NULL
+ *   ws      device workspace of at least pi_workspace_bytes(layer, B) bytes
+ * 1 <= B <= PI_MAX_BATCH.  At least one of mask/logits must be non-NULL. */
+pi_status pi_predict(pi_layer *layer, const uint16_t *x, int32_t B,
+                     uint8_t *mask, float *logits, void *ws, size_t ws_bytes,
+                     void *stream);
+
+/* Active-index compaction (section 2.3, core module 4 computes on the
+ * predicted neurons directly; section 4.4 limitation 3: with a batch, the set
+ * is the union over the batch):
+ *   idx[0..count) = ascending positions i with mask[b, i] != 0 for some b.
+ *   mask   device uint8 [B, ffn]
+ *   idx    device int32 [ffn]   (entries past count are left untouched)
+ *   count  device int32 [1] */
+pi_status pi_compact_active(const pi_layer *layer, const uint8_t *mask,
+                            int32_t B, int32_t *idx, int32_t *count,
+                            void *stream);
+
+/* Neuron-aware sparse FFN (section 2.3, core module 4; variable table,
+ * "sparsity": neurons outside the set contribute exactly nothing):
+ *   for k < *count, i = idx[k]:  a_i(b) per the layer's activation
+ *   y[b, :] = sum_k a_{idx[k]}(b) * W_down^T[idx[k], :]
+ * Only the rows idx[0..count) of W_up (and W_gate), and of W_down^T, are read.
+ * binary32 accumulation; the reduction over neurons is split over CTAs and
+ * combined in a fixed order, so results are bitwise reproducible run to run.
+ *   x      device fp16 [B, d]
+ *   idx    device int32 [>= *count], positions in [0, ffn), any order
+ *   count  device int32 [1], 0 <= *count <= ffn
+ *   y      device fp32 [B, d], overwritten
+ * Out-of-range idx entries are skipped and *count is clamped to [0, ffn];
+ * either sets the layer's device status. */
+pi_status pi_sparse_ffn(pi_layer *layer, const uint16_t *x, int32_t B,
+                        const int32_t *idx, const int32_t *count, float *y,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/* Dense comparator: the same kernels as pi_sparse_ffn over every neuron
+ * (idx = 0..ffn-1), without the predictor. */
+pi_status pi_ffn_dense_ref(pi_layer *layer, const uint16_t *x, int32_t B,
+                           float *y, void *ws, size_t ws_bytes, void *stream);
+
+/* The whole layer for one batch: pi_predict, pi_compact_active and
+ * pi_sparse_ffn in sequence, with the mask kept in the workspace.
+ *   idx, count  device outputs as in pi_compact_active
+ *   y           device fp32 [B, d] */
+pi_status pi_layer_forward(pi_layer *layer, const uint16_t *x, int32_t B,
+                           int32_t *idx, int32_t *count, float *y,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* Offline activation profile (section 2.3, core module 1 "LLM profiler";
+ * section 2.2, profiling data): for T tokens x_t, in model space,
+ *   counts[i] += #{t : z_i(x_t) > 0}, z = W_up x + b (ReLU) or W_gate x + b (ReGLU)
+ *   x       device fp16 [T, d]
+ *   counts  device int32 [ffn], accumulated into (the caller zeroes it)
+ * Reads the desc's model-space weights; needs no layer object. */
+pi_status pi_profile_activations(const pi_layer_desc *desc, const uint16_t *x,
+                                 int32_t T, int32_t *counts, void *stream);
+
+/* Hot-first order from a profile (section 2.3, variable table: impact
+ * v_i = f_i; hot neurons are the frequently activated ones): perm lists the
+ * neurons by count descending, ties by ascending index.  Host arrays. */
+pi_status pi_hot_first_perm(const int32_t *counts, int32_t ffn, int32_t *perm);
+
+/* Profiling hook.  While ev_before / ev_after (cudaEvent_t passed as void*)
+ * are set, each pi_sparse_ffn, pi_ffn_dense_ref and pi_layer_forward call on
+ * this layer records ev_before on its stream immediately before the main
+ * up/down kernel and ev_after immediately after it (as external event-record
+ * nodes when the stream is being captured into a CUDA graph), so the
+ * caller can time that kernel alone with cudaEventElapsedTime.  Both NULL
+ * switches it off.  The setting is per layer and read at call time. */
+pi_status pi_layer_set_timing_events(pi_layer *layer, void *ev_before, void *ev_after);
+
+/* Number of kernel launches one pi_layer_forward call makes for a batch of B
+ * tokens (0 on bad arguments). */
+int32_t pi_forward_launches(const pi_layer *layer, int32_t B);
+
+/* Synchronize `stream`, then return PI_ERR_DEVICE_CHECK if any kernel on this
+ * layer flagged an out-of-range index or count since the last query (and
+ * clear the flag), else PI_OK. */
+pi_status pi_device_status(pi_layer *layer, void *stream);
+
+/* Thread-local text of the last error ("" if none). */
+const char *pi_last_error(void);
+
+/* Name of a status code. */
+const char *pi_status_string(pi_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PI_H_ */
