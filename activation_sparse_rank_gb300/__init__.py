@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     lib,
     lib_path,
     profile_activations,
+    stack_forward,
 )
 
 __all__ = [
@@ -27,4 +28,5 @@ __all__ = [
     "lib",
     "lib_path",
     "profile_activations",
+    "stack_forward",
 ]

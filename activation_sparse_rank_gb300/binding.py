@@ -50,6 +50,7 @@ _SIG = {
     "pi_sparse_ffn": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
     "pi_ffn_dense_ref": (C.c_int, [_p, _p, _i32, _p, _p, C.c_size_t, _p]),
     "pi_layer_forward": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
+    "pi_stack_forward": (C.c_int, [_p, _i32, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
     "pi_profile_activations": (C.c_int, [C.POINTER(pi_layer_desc), _p, _i32, _p, _p]),
     "pi_hot_first_perm": (C.c_int, [_p, _i32, _p]),
     "pi_device_status": (C.c_int, [_p, _p]),
@@ -245,6 +246,21 @@ class Layer:
     def device_status(self, stream=None) -> int:
         """0 if no kernel flagged bad input since the last query, else the status code."""
         return int(lib.pi_device_status(self._h, _stream(stream)))
+
+
+def stack_forward(layers, x, y, idx=None, count=None, ws=None, stream=None, handles=None):
+    """Run layers in order on x [n_layers, B, d] fp16 into y [n_layers, B, d] fp32.
+    `handles` may carry a prebuilt ctypes array of the layer handles."""
+    n = len(layers)
+    _req(x, torch.float16, "x")
+    B = x.shape[1]
+    if handles is None:
+        handles = (C.c_void_p * n)(*[l.handle.value for l in layers])
+    if ws is None:
+        ws = layers[0].workspace(B)
+    _check(lib.pi_stack_forward(handles, n, _ptr(x), B, _ptr(idx), _ptr(count), _ptr(y),
+                                _ptr(ws), ws.numel(), _stream(stream)), "pi_stack_forward")
+    return y
 
 
 def profile_activations(t: dict, x: torch.Tensor, counts: Optional[torch.Tensor] = None,

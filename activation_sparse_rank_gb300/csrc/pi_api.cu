@@ -176,6 +176,9 @@ WsLayout ws_layout(const pi_layer *L, int B) {
   w.mask = off;    off += align_up((size_t)B * L->ffn);
   w.idx = off;     off += align_up(sizeof(int32_t) * (size_t)L->ffn);
   w.count = off;   off += align_up(sizeof(int32_t) * 4);
+  w.cnt = off;     off += align_up(sizeof(int32_t) * (size_t)step_grid(L));
+  w.lists = off;   off += align_up(sizeof(int32_t) * (size_t)step_grid(L) * step_slice(L));
+  w.bar = off;     off += align_up(sizeof(unsigned));
   w.total = off;
   return w;
 }
@@ -433,11 +436,59 @@ pi_status pi_layer_forward(pi_layer *L, const uint16_t *x, int32_t B, int32_t *i
   if (!y || !aligned16(y)) return pi::fail(PI_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *wsb = static_cast<char *>(ws);
-  uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
   const __half *xh = reinterpret_cast<const __half *>(x);
+  if (B <= 2) {
+    PI_TRY_CUDA(pi::run_stack(&L, 1, xh, B, idx, count, y, w, wsb, s));
+    return PI_OK;
+  }
+  uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
   PI_TRY_CUDA(pi::run_predict(L, xh, B, mask, nullptr, reinterpret_cast<float *>(wsb + w.h), s));
   PI_TRY_CUDA(pi::run_compact(L, mask, B, idx, count, s));
   PI_TRY_CUDA(pi::run_sparse_ffn(L, xh, B, idx, count, 0, y, w, wsb, s));
+  return PI_OK;
+}
+
+pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint16_t *x,
+                           int32_t B, int32_t *idx, int32_t *count, float *y, void *ws,
+                           size_t ws_bytes, void *stream) {
+  g_err[0] = 0;
+  if (!layers || n_layers < 1) return pi::fail(PI_ERR_INVALID_ARG, "layers is NULL or n_layers < 1");
+  for (int l = 0; l < n_layers; ++l) {
+    const pi_layer *Ll = layers[l];
+    if (!Ll) return pi::fail(PI_ERR_INVALID_ARG, "layers[%d] is NULL", l);
+    if (Ll->d != layers[0]->d || Ll->ffn != layers[0]->ffn || Ll->rank != layers[0]->rank ||
+        Ll->act != layers[0]->act || Ll->device != layers[0]->device)
+      return pi::fail(PI_ERR_INVALID_ARG, "layers[%d] differs in shape, activation or device", l);
+  }
+  pi_layer *L = layers[0];
+  pi::WsLayout w;
+  pi_status st = check_common(L, x, B, ws, ws_bytes, &w);
+  if (st != PI_OK) return st;
+  if (!y || !aligned16(y)) return pi::fail(PI_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
+  if ((idx && !aligned4(idx)) || (count && !aligned4(count)))
+    return pi::fail(PI_ERR_INVALID_ARG, "idx and count must be 4-byte aligned");
+  if (B > 2 && (!idx || !count))
+    return pi::fail(PI_ERR_INVALID_ARG, "B > 2 needs idx and count buffers");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *wsb = static_cast<char *>(ws);
+  const __half *xh = reinterpret_cast<const __half *>(x);
+  const size_t xs = (size_t)B * L->d;
+  if (B <= 2) {
+    for (int l0 = 0; l0 < n_layers; l0 += pi::kMaxStack) {
+      const int n = std::min(pi::kMaxStack, n_layers - l0);
+      PI_TRY_CUDA(pi::run_stack(layers + l0, n, xh + l0 * xs, B, idx ? idx + (size_t)l0 * L->ffn : nullptr,
+                                count ? count + l0 : nullptr, y + l0 * xs, w, wsb, s));
+    }
+    return PI_OK;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    pi_layer *Ll = layers[l];
+    uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
+    PI_TRY_CUDA(pi::run_predict(Ll, xh + l * xs, B, mask, nullptr, reinterpret_cast<float *>(wsb + w.h), s));
+    PI_TRY_CUDA(pi::run_compact(Ll, mask, B, idx + (size_t)l * L->ffn, count + l, s));
+    PI_TRY_CUDA(pi::run_sparse_ffn(Ll, xh + l * xs, B, idx + (size_t)l * L->ffn, count + l, 0,
+                                   y + l * xs, w, wsb, s));
+  }
   return PI_OK;
 }
 
@@ -477,8 +528,9 @@ pi_status pi_layer_set_timing_events(pi_layer *L, void *ev_before, void *ev_afte
 
 int32_t pi_forward_launches(const pi_layer *L, int32_t B) {
   if (!L || B < 1 || B > PI_MAX_BATCH) return 0;
-  // predict_h, predict_l, compact, then fused + reduce (B <= 2) or up + down + reduce
-  return B <= 2 ? 5 : 6;
+  // B <= 2: one persistent cooperative launch (after a barrier-counter memset);
+  // otherwise predict_h, predict_l, compact, up, down, reduce
+  return B <= 2 ? 1 : 6;
 }
 
 pi_status pi_device_status(pi_layer *L, void *stream) {
@@ -490,9 +542,10 @@ pi_status pi_device_status(pi_layer *L, void *stream) {
   PI_TRY_CUDA(cudaMemcpy(&v, L->status, sizeof(v), cudaMemcpyDeviceToHost));
   if (v) {
     PI_TRY_CUDA(cudaMemset(L->status, 0, sizeof(v)));
-    return pi::fail(PI_ERR_DEVICE_CHECK, "device check failed:%s%s",
+    return pi::fail(PI_ERR_DEVICE_CHECK, "device check failed:%s%s%s",
                     (v & PI_STATUS_BAD_INDEX) ? " index out of range" : "",
-                    (v & PI_STATUS_BAD_COUNT) ? " count out of range" : "");
+                    (v & PI_STATUS_BAD_COUNT) ? " count out of range" : "",
+                    (v & PI_STATUS_BARRIER_TIMEOUT) ? " grid barrier timed out" : "");
   }
   return PI_OK;
 }

@@ -12,6 +12,7 @@
 // Device status bits (set with atomicOr, read and cleared by pi_device_status).
 #define PI_STATUS_BAD_INDEX 1u
 #define PI_STATUS_BAD_COUNT 2u
+#define PI_STATUS_BARRIER_TIMEOUT 4u
 
 struct pi_layer {
   int d = 0, ffn = 0, rank = 0, act = 0;
@@ -51,8 +52,42 @@ struct WsLayout {
   size_t mask = 0;     // uint8 [B, ffn]
   size_t idx = 0;      // int32 [ffn]           (pi_layer_forward when idx not given)
   size_t count = 0;    // int32 [4]
+  size_t cnt = 0;      // int32 [G]             per-CTA active counts (persistent step)
+  size_t lists = 0;    // int32 [G, slice]      per-CTA local active lists
+  size_t bar = 0;      // uint32                grid-barrier counter
   size_t total = 0;
 };
+
+// Layers per persistent launch (longer stacks are split into several launches).
+constexpr int kMaxStack = 64;
+
+// Device pointers of one layer, as the persistent kernel sees them.
+struct LayerDev {
+  const __half *W_p1, *W_p2, *W_up, *W_gate, *W_dT;
+  const float *b, *c_p;
+};
+
+// Kernel parameters of the persistent step (passed by value, < 4 KB).
+struct StackParams {
+  int n_layers, d, ffn, rank;
+  int G, slice, lanes_l, sub, pf_rows, pf_next;
+  const __half *x;       // [n_layers, B, d]
+  float *y;              // [n_layers, B, d]
+  int32_t *idx;          // [n_layers, ffn] or nullptr
+  int32_t *count;        // [n_layers] or nullptr
+  float *h;              // scratch [B, rank]
+  int32_t *cnt;          // scratch [G]
+  int32_t *lists;        // scratch [G, slice]
+  float *partial;        // scratch [G, B, d]
+  unsigned *bar;         // scratch barrier counter (zeroed before launch)
+  unsigned *status;
+  LayerDev layers[kMaxStack];
+};
+int step_grid(const pi_layer *L);
+int step_slice(const pi_layer *L);
+size_t step_smem(const pi_layer *L, int B);
+cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, int32_t *idx,
+                      int32_t *count, float *y, const WsLayout &w, char *ws, cudaStream_t s);
 WsLayout ws_layout(const pi_layer *L, int B);
 int fused_splits(const pi_layer *L);        // CTAs of the batch-1 fused kernel
 int down_splits(const pi_layer *L, int B);  // split count of the generic down kernel

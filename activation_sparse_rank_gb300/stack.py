@@ -1,20 +1,20 @@
 """A stack of sparse-FFN layers run in decode order, captured as a CUDA graph.
 
 One step feeds T tokens (each a batch of B rows) through the L layers in
-sequence: for token t and layer l, ``pi_layer_forward`` computes the predictor,
-the active list and the sparse FFN of x[t, l] into y[t, l].  The active count
-of every (token, layer) is kept on the device, so touched bytes can be
-counted after the step without any host round trip inside it.  The whole
-step is one graph launch; successive kernels are chained with programmatic
-dependent launch inside libpi.
+sequence: token t is one ``pi_stack_forward`` call over all layers (for
+B <= 2 a single persistent cooperative kernel), reading x[t] [L, B, d] and
+writing y[t] [L, B, d].  The active count of every (token, layer) stays on
+the device, so touched bytes can be counted after the step without any host
+round trip inside it.  The whole step is one graph launch.
 """
 from __future__ import annotations
 
+import ctypes as C
 from typing import List, Optional
 
 import torch
 
-from .binding import Layer
+from .binding import Layer, stack_forward
 
 
 class SparseFFNStack:
@@ -26,48 +26,53 @@ class SparseFFNStack:
         self.T = int(tokens)
         self.B = int(B)
         self.d = layers[0].d
-        self.ffn_max = max(l.ffn for l in layers)
+        self.ffn = layers[0].ffn
         dev = layers[0].device
         self.device = dev
-        self.ws = torch.empty(max(l.workspace_bytes(B) for l in layers), dtype=torch.uint8,
-                              device=dev)
-        self.idx = torch.empty(self.L, self.ffn_max, dtype=torch.int32, device=dev)
+        self.ws = layers[0].workspace(B)
+        self.idx = torch.empty(self.L, self.ffn, dtype=torch.int32, device=dev)
         self.count = torch.zeros(self.T, self.L, dtype=torch.int32, device=dev)
         self.x = torch.empty(self.T, self.L, B, self.d, dtype=torch.float16, device=dev)
         self.y = torch.empty(self.T, self.L, B, self.d, dtype=torch.float32, device=dev)
+        self.handles = (C.c_void_p * self.L)(*[l.handle.value for l in layers])
         self.graph: Optional[torch.cuda.CUDAGraph] = None
         self.stream = torch.cuda.Stream(device=dev)
 
     def launches_per_step(self) -> int:
-        return sum(l.forward_launches(self.B) for l in self.layers) * self.T
+        """Kernels of this library launched per step (memsets not counted)."""
+        per_token = 1 if self.B <= 2 else sum(l.forward_launches(self.B) for l in self.layers)
+        n_launch = -(-self.L // 64) if self.B <= 2 else 1
+        return per_token * n_launch * self.T
+
+    def _token(self, t: int, stream):
+        stack_forward(self.layers, self.x[t], self.y[t], idx=self.idx, count=self.count[t],
+                      ws=self.ws, stream=stream, handles=self.handles)
 
     def enqueue(self, stream=None, tokens=None):
         """Enqueue the step (all tokens, all layers) on `stream` without a graph."""
         for t in range(self.T if tokens is None else tokens):
-            for li, layer in enumerate(self.layers):
-                layer.forward(self.x[t, li], self.idx[li], self.count[t, li:li + 1],
-                              self.y[t, li], ws=self.ws, stream=stream)
+            self._token(t, stream)
 
-    def capture(self, timing_events=None):
+    def capture(self, timing_events=None, tokens=None):
         """Capture one step as a CUDA graph.  timing_events: optional dict
-        {(t, l): (before, after)} of external torch events recorded around the
-        main up/down kernel of those launches."""
+        {t: (before, after)} of external torch events recorded around the main
+        kernel of token t."""
+        T = self.T if tokens is None else tokens
         s = self.stream
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.enqueue(stream=s)            # warm-up outside capture (same work)
+            self.enqueue(stream=s, tokens=T)       # warm-up outside capture (same work)
         s.synchronize()
         g = torch.cuda.CUDAGraph()
+        first = self.layers[0]
         with torch.cuda.graph(g, stream=s):
-            for t in range(self.T):
-                for li, layer in enumerate(self.layers):
-                    ev = timing_events.get((t, li)) if timing_events else None
-                    if ev is not None:
-                        layer.set_timing_events(*ev)
-                    layer.forward(self.x[t, li], self.idx[li], self.count[t, li:li + 1],
-                                  self.y[t, li], ws=self.ws, stream=s)
-                    if ev is not None:
-                        layer.set_timing_events(None, None)
+            for t in range(T):
+                ev = timing_events.get(t) if timing_events else None
+                if ev is not None:
+                    first.set_timing_events(*ev)
+                self._token(t, s)
+                if ev is not None:
+                    first.set_timing_events(None, None)
         return g
 
     def build_graph(self):

@@ -336,51 +336,52 @@ def main():
     torch.cuda.synchronize()
     dense_tok_s = 3 * Td / (e0.elapsed_time(e1) / 1000.0)
 
-    # dominant kernel (fused up/down) timed inside a captured step
-    Tr = min(32, T)
+    # dominant kernel (the persistent step kernel, one launch per token)
+    # timed inside a captured step with external event-record nodes
+    Tr = min(64, T)
     try:
-        evs = {(t, l): (torch.cuda.Event(enable_timing=True, external=True),
-                        torch.cuda.Event(enable_timing=True, external=True))
-               for t in range(Tr) for l in range(n_layers)}
+        evs = {t: (torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True)) for t in range(Tr)}
+        how = "external event-record nodes around each launch inside a captured step"
+    except TypeError:
+        evs = None
+        how = None
+    if evs is not None:
         for a, b in evs.values():      # materialise the events before capture
             a.record(s); b.record(s)
         s.synchronize()
-        save = stack.T
-        stack.T = Tr
-        g_inst = stack.capture(timing_events=evs)
-        stack.T = save
+        g_inst = stack.capture(timing_events=evs, tokens=Tr)
         with torch.cuda.stream(s):
             g_inst.replay()
         s.synchronize()
-        how = "external event-record nodes around each launch inside a captured step"
-    except TypeError:
-        evs = {(t, l): (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for t in range(Tr) for l in range(n_layers)}
+    else:
+        evs = {t: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for t in range(Tr)}
         with torch.cuda.stream(s):
             for t in range(Tr):
-                for li, layer in enumerate(layers):
-                    layer.set_timing_events(*evs[(t, li)])
-                    layer.forward(stack.x[t, li], stack.idx[li], stack.count[t, li:li + 1],
-                                  stack.y[t, li], ws=ws, stream=s)
-                    layer.set_timing_events(None, None)
+                layers[0].set_timing_events(*evs[t])
+                stack._token(t, s)
+                layers[0].set_timing_events(None, None)
         s.synchronize()
         how = "events around each launch, eager step"
-    k_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in sorted(evs)]
+    k_ms = [evs[t][0].elapsed_time(evs[t][1]) for t in range(Tr)]
     cnt = stack.count[:Tr].cpu().numpy()
-    alg_bytes = float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act)
+    alg_bytes = (Tr * n_layers * predictor_bytes(spec.d, spec.ffn, spec.rank)
+                 + float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act))
     k_avg_ms = sum(k_ms) / len(k_ms)
     achieved = alg_bytes / len(k_ms) / (k_avg_ms / 1e3) / 1e9
     traffic = None
-    tfile = ROOT / "profiles" / "fused_traffic.json"
+    tfile = ROOT / "profiles" / "stack_step_traffic.json"
     if tfile.exists():
         tj = json.loads(tfile.read_text())
         if tj.get("kernel_source_hash") == kernel_source_hash():
             traffic = tj.get("bytes_per_launch")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "k_fused_small (up+down over the active list)",
+                "kernel": f"k_stack_step (one token through {n_layers} layers)",
                 "peak_kind": peak_kind + " (copy bandwidth)",
                 "launches_timed": len(k_ms), "avg_launch_us": k_avg_ms * 1e3,
+                "algorithmic_bytes_per_launch": alg_bytes / len(k_ms),
                 "timing": how}
 
     # end to end from pinned host buffers through the public API

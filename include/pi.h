@@ -159,13 +159,34 @@ pi_status pi_sparse_ffn(pi_layer *layer, const uint16_t *x, int32_t B,
 pi_status pi_ffn_dense_ref(pi_layer *layer, const uint16_t *x, int32_t B,
                            float *y, void *ws, size_t ws_bytes, void *stream);
 
-/* The whole layer for one batch: pi_predict, pi_compact_active and
- * pi_sparse_ffn in sequence, with the mask kept in the workspace.
+/* The whole layer for one batch: the results of pi_predict, then
+ * pi_compact_active, then pi_sparse_ffn.  For B <= 2 this is one persistent
+ * cooperative kernel (see pi_stack_forward); for larger B the three stages.
  *   idx, count  device outputs as in pi_compact_active
  *   y           device fp32 [B, d] */
 pi_status pi_layer_forward(pi_layer *layer, const uint16_t *x, int32_t B,
                            int32_t *idx, int32_t *count, float *y,
                            void *ws, size_t ws_bytes, void *stream);
+
+/* A decode step through a stack of layers in order (layer l reads x[l] and
+ * writes y[l]; each layer's result is complete before the next layer
+ * starts, as when the next input depends on it).  All layers must share d,
+ * ffn, rank, activation and device.
+ *   layers  host array of n_layers layer objects
+ *   x       device fp16 [n_layers, B, d]
+ *   idx     device int32 [n_layers, ffn] active lists, or NULL (B <= 2 only)
+ *   count   device int32 [n_layers] active counts, or NULL (B <= 2 only)
+ *   y       device fp32 [n_layers, B, d]
+ *   ws      workspace of pi_workspace_bytes(layers[0], B) bytes
+ * For B <= 2 each group of up to 64 layers is one cooperative launch with one
+ * CTA per SM and four grid-wide barriers per layer (predictor hidden layer,
+ * active counts, partial sums, output).  Barrier waits are bounded: a wait
+ * that runs out sets a status bit (PI_ERR_DEVICE_CHECK from
+ * pi_device_status on layers[0]) and the kernel returns. */
+pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers,
+                           const uint16_t *x, int32_t B, int32_t *idx,
+                           int32_t *count, float *y, void *ws,
+                           size_t ws_bytes, void *stream);
 
 /* Offline activation profile (section 2.3, core module 1 "LLM profiler";
  * section 2.2, profiling data): for T tokens x_t, in model space,
@@ -182,12 +203,14 @@ pi_status pi_profile_activations(const pi_layer_desc *desc, const uint16_t *x,
 pi_status pi_hot_first_perm(const int32_t *counts, int32_t ffn, int32_t *perm);
 
 /* Profiling hook.  While ev_before / ev_after (cudaEvent_t passed as void*)
- * are set, each pi_sparse_ffn, pi_ffn_dense_ref and pi_layer_forward call on
- * this layer records ev_before on its stream immediately before the main
- * up/down kernel and ev_after immediately after it (as external event-record
- * nodes when the stream is being captured into a CUDA graph), so the
- * caller can time that kernel alone with cudaEventElapsedTime.  Both NULL
- * switches it off.  The setting is per layer and read at call time. */
+ * are set, each call on this layer records ev_before on its stream
+ * immediately before its main kernel and ev_after immediately after it (as
+ * external event-record nodes when the stream is being captured into a CUDA
+ * graph), so the caller can time that kernel alone with cudaEventElapsedTime.
+ * The main kernel is the up/down kernel of pi_sparse_ffn / pi_ffn_dense_ref
+ * (and of pi_layer_forward for B > 2), and the persistent step kernel of
+ * pi_layer_forward / pi_stack_forward for B <= 2 (hook of layers[0]).  Both
+ * NULL switches it off.  The setting is per layer and read at call time. */
 pi_status pi_layer_set_timing_events(pi_layer *layer, void *ev_before, void *ev_after);
 
 /* Number of kernel launches one pi_layer_forward call makes for a batch of B

@@ -1,0 +1,154 @@
+"""Parity of the multi-layer decode step (pi_stack_forward, persistent kernel)
+and of the full-size workloads, against the float64 CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import ffn as O
+from tests.gpu_helpers import check_union_set, check_y, oracle_y_for_valid_set, to_dev
+from workload import CONFIGS, LayerSpec, config_by_name, make_layer, make_tokens, sub_seed
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pi():
+    import __graft_entry__
+    __graft_entry__.build()
+    import activation_sparse_rank_gb300 as pi
+    return pi
+
+
+def _stack(pi, spec, n, seed, perms=None):
+    ts = [make_layer(spec, seed, l) for l in range(n)]
+    layers = [pi.Layer.from_dict(to_dev(t), perm=None if perms is None else perms[l])
+              for l, t in enumerate(ts)]
+    return ts, layers
+
+
+def _check_layer(t, x, y, S, perm=None):
+    L = O.OracleLayer.from_tensors(t)
+    if perm is not None:
+        L = O.permute_layer(L, perm)
+    r = O.predicted_forward(L, x)
+    band = check_union_set(S, r["l"], r["tau"])
+    check_y(y, oracle_y_for_valid_set(L, x, S))
+    return band
+
+
+@pytest.mark.parametrize("act,d,ffn,r", [("relu", 1024, 4096, 64), ("reglu", 2048, 3000, 40),
+                                         ("relu", 12288, 2000, 128)])
+@pytest.mark.parametrize("B", [1, 2, 3])
+def test_stack_forward(pi, act, d, ffn, r, B):
+    n = 3
+    spec = LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1)
+    ts, layers = _stack(pi, spec, n, seed=d + ffn)
+    x = make_tokens(d, n * B, seed=3).view(n, B, d)
+    y = torch.empty(n, B, d, dtype=torch.float32, device="cuda")
+    idx = torch.full((n, ffn), -1, dtype=torch.int32, device="cuda")
+    count = torch.empty(n, dtype=torch.int32, device="cuda")
+    pi.stack_forward(layers, x.cuda(), y, idx=idx, count=count)
+    y2 = torch.empty_like(y)
+    pi.stack_forward(layers, x.cuda(), y2, idx=idx, count=count)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    for l in range(n):
+        c = int(count[l].item())
+        S = idx[l, :c].cpu().numpy().astype(np.int64)
+        _check_layer(ts[l], x[l], y[l].cpu().numpy(), S)
+    assert layers[0].device_status() == 0
+
+
+def test_long_stack_spans_launches(pi):
+    """More layers than one persistent launch holds."""
+    n, d, ffn, r = 70, 256, 512, 16
+    spec = LayerSpec(d=d, ffn=ffn, rank=r, mean_f=0.15)
+    ts, layers = _stack(pi, spec, n, seed=5)
+    x = make_tokens(d, n, seed=6).view(n, 1, d)
+    y = torch.empty(n, 1, d, dtype=torch.float32, device="cuda")
+    idx = torch.empty((n, ffn), dtype=torch.int32, device="cuda")
+    count = torch.empty(n, dtype=torch.int32, device="cuda")
+    pi.stack_forward(layers, x.cuda(), y, idx=idx, count=count)
+    torch.cuda.synchronize()
+    for l in range(n):
+        c = int(count[l].item())
+        _check_layer(ts[l], x[l], y[l].cpu().numpy(), idx[l, :c].cpu().numpy().astype(np.int64))
+    assert layers[0].device_status() == 0
+
+
+def test_graph_replay_matches_eager(pi):
+    from activation_sparse_rank_gb300.stack import SparseFFNStack
+    spec = LayerSpec(d=1024, ffn=4096, rank=64, mean_f=0.1)
+    ts, layers = _stack(pi, spec, 4, seed=8)
+    st = SparseFFNStack(layers, tokens=5, B=1)
+    st.x.copy_(make_tokens(1024, 20, seed=9).view(5, 4, 1, 1024).cuda())
+    st.enqueue(stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    y_eager = st.y.clone()
+    st.y.zero_()
+    st.build_graph()
+    st.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(st.y, y_eager)
+    xh = st.x.cpu().pin_memory()
+    yh = torch.empty(st.y.shape, dtype=torch.float32).pin_memory()
+    st.run_host(xh, yh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y_eager.cpu())
+
+
+def test_bench_configuration_sampled(pi):
+    """The OPT-7B-shaped stack exactly as the benchmark builds and times it
+    (32 layers, hot-first order from a 10k-token profile, graph replay of the
+    persistent step), checked on sampled (token, layer) pairs."""
+    import bench
+    from activation_sparse_rank_gb300.stack import SparseFFNStack
+    cfg = config_by_name("opt7b_stack")
+    spec = cfg.layer
+    dev = torch.device("cuda")
+    check_layers = [0, 13, 31]
+    layers, _ = bench.build_stack(cfg, dev, cfg.layers, keep_host_layers=0)
+    T = 3
+    st = SparseFFNStack(layers, tokens=T, B=1)
+    X = make_tokens(spec.d, T * cfg.layers, sub_seed(cfg.seed, 1000, "bench_x"), dev)
+    st.x.copy_(X.view(T, cfg.layers, 1, spec.d))
+    st.build_graph()
+    st.replay()
+    torch.cuda.synchronize()
+    assert layers[0].device_status() == 0
+    for l in check_layers:
+        t = make_layer(spec, cfg.seed, l, device=dev)
+        perm = layers[l].perm()
+        t = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+        tok = T - 1                     # the active lists hold the last token's sets
+        c = int(st.count[tok, l].item())
+        S = st.idx[l, :c].cpu().numpy().astype(np.int64)
+        _check_layer(t, st.x[tok, l].cpu(), st.y[tok, l].cpu().numpy(), S, perm=perm)
+        # profile order: hot-first permutation is a permutation sorted by the GPU profile
+        assert sorted(perm.tolist()) == list(range(spec.ffn))
+
+
+@pytest.mark.parametrize("name", ["llama2_70b_reglu", "falcon40b_stack", "opt175b_stack"])
+def test_full_size_layer(pi, name):
+    """One layer at the full per-layer size of each larger workload, batch 1
+    through the persistent step, plus the workload's larger batches through
+    the batched path (union active set)."""
+    cfg = config_by_name(name)
+    spec = cfg.layer
+    dev = torch.device("cuda")
+    t = make_layer(spec, cfg.seed, 0, device=dev)
+    layer = pi.Layer.from_dict(t)
+    th = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    del t
+    L = O.OracleLayer.from_tensors(th)
+    for B in sorted(set((1,) + tuple(b for b in cfg.batches if b > 1))):
+        x = make_tokens(spec.d, B, seed=sub_seed(cfg.seed, B, "full_size_x"))
+        y, idx, count = layer.forward(x.to(dev))
+        torch.cuda.synchronize()
+        S = idx[:int(count.item())].cpu().numpy().astype(np.int64)
+        h = O.predictor_hidden(L, x)
+        check_union_set(S, O.predictor_logits(L, h), O.logit_error_bound(L, x, h))
+        rows = [0, B - 1] if B > 2 else list(range(B))
+        y_ref = O.sparse_ffn(L, x[rows], S)
+        check_y(y.cpu().numpy()[rows], y_ref)
+    assert layer.device_status() == 0
