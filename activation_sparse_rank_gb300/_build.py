@@ -17,7 +17,7 @@ PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
 CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
-OUT = PKG / "_lib"
+OUT = Path(os.environ.get("PI_BUILD_DIR", str(PKG / "_lib")))
 LIB = OUT / "libpi.so"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -14,8 +14,10 @@ from typing import Optional
 import numpy as np
 import torch
 
+import os
+
 _HERE = Path(__file__).resolve().parent
-lib_path = _HERE / "_lib" / "libpi.so"
+lib_path = Path(os.environ.get("PI_LIB_PATH", str(_HERE / "_lib" / "libpi.so")))
 
 if not lib_path.exists():
     raise ImportError(

@@ -68,6 +68,23 @@ __device__ bool grid_barrier(unsigned *bar, unsigned epoch, unsigned *status) {
   return ok_s != 0;
 }
 
+#ifdef PI_PHASE_TIMING
+// Diagnostic build only: globaltimer stamps at phase boundaries of CTA 0 and
+// CTA G-1 for the first 16 layers of the most recent launch.
+__device__ unsigned long long g_phase_ts[3][16][16];
+#define PHASE_STAMP(l, ph)                                                        \
+  do {                                                                            \
+    const int w_ = blockIdx.x == 0 ? 0 : blockIdx.x == gridDim.x / 2 ? 1 : blockIdx.x == gridDim.x - 1 ? 2 : -1; \
+    if (threadIdx.x == 0 && w_ >= 0 && (l) < 16) {                               \
+      unsigned long long t_;                                                      \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                      \
+      g_phase_ts[w_][l][ph] = t_;                                                 \
+    }                                                                             \
+  } while (0)
+#else
+#define PHASE_STAMP(l, ph) do {} while (0)
+#endif
+
 template <int CPT, int NB, bool REGLU>
 __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constant__ pi::StackParams p) {
   constexpr int G1 = CPT == 1 ? 16 : 8 / CPT > 0 ? 8 / CPT : 1;     // phase-E loads per group
@@ -110,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
                           : make_uint4(0, 0, 0, 0);
       }
 
+    PHASE_STAMP(l, 0);
     // ---------------- A: h = ReLU(W_p1 x), rows cta, cta + G, ...
     for (int k0 = cta; k0 < r; k0 += 2 * G) {
       uint4 w[2][CPT];
@@ -146,11 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       }
       __syncthreads();
     }
+    PHASE_STAMP(l, 1);
     if (!grid_barrier(p.bar, ++epoch, status)) return;
+    PHASE_STAMP(l, 2);
 
     // ---------------- C: logits over my slice, local ordered active list
     for (int e = tid; e < NB * r; e += kThreads) h_s[e] = ldcg(p.h + e);
     __syncthreads();
+    PHASE_STAMP(l, 3);
     {
       const int GL = p.lanes_l;                 // lanes per predictor row (8, 16, 32)
       const int rows_per_warp = 32 / GL;
@@ -158,43 +179,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       const int nvr = r >> 3;
       const int n_rows = s1 - s0;
       const int iters = (n_rows + kWarps * rows_per_warp - 1) / (kWarps * rows_per_warp);
-      for (int it = 0; it < iters; ++it) {
-        const int rl = (it * kWarps + wid) * rows_per_warp + lane / GL;
-        const bool valid = rl < n_rows;
-        float acc[NB];
+      constexpr int RU = 8;                     // rows in flight per lane
+      for (int it0 = 0; it0 < iters; it0 += RU) {
+        float acc[RU][NB];
 #pragma unroll
-        for (int t = 0; t < NB; ++t) acc[t] = 0.f;
-        if (valid) {
-          const uint4 *wrow = reinterpret_cast<const uint4 *>(Ld.W_p2 + (size_t)(s0 + rl) * r);
-          for (int v = sub; v < nvr; v += GL) {
-            const uint4 wv = pidev::ld_stream(wrow + v);
+        for (int u = 0; u < RU; ++u)
 #pragma unroll
-            for (int t = 0; t < NB; ++t) {
-              const float4 *hp = reinterpret_cast<const float4 *>(h_s + t * r + v * 8);
-              const float4 h0 = hp[0], h1 = hp[1];
-              const __half2 *wh = reinterpret_cast<const __half2 *>(&wv);
+          for (int t = 0; t < NB; ++t) acc[u][t] = 0.f;
+        for (int v = sub; v < nvr; v += GL) {
+          uint4 wv[RU];
+#pragma unroll
+          for (int u = 0; u < RU; ++u) {
+            const int rl = ((it0 + u) * kWarps + wid) * rows_per_warp + lane / GL;
+            wv[u] = (it0 + u < iters && rl < n_rows)
+                        ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p2 + (size_t)(s0 + rl) * r) + v)
+                        : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int t = 0; t < NB; ++t) {
+            const float4 *hp = reinterpret_cast<const float4 *>(h_s + t * r + v * 8);
+            const float4 h0 = hp[0], h1 = hp[1];
+#pragma unroll
+            for (int u = 0; u < RU; ++u) {
+              const __half2 *wh = reinterpret_cast<const __half2 *>(&wv[u]);
               const float2 w0 = __half22float2(wh[0]), w1 = __half22float2(wh[1]);
               const float2 w2 = __half22float2(wh[2]), w3 = __half22float2(wh[3]);
-              float a = acc[t];
+              float a = acc[u][t];
               a = fmaf(w0.x, h0.x, a); a = fmaf(w0.y, h0.y, a);
               a = fmaf(w1.x, h0.z, a); a = fmaf(w1.y, h0.w, a);
               a = fmaf(w2.x, h1.x, a); a = fmaf(w2.y, h1.y, a);
               a = fmaf(w3.x, h1.z, a); a = fmaf(w3.y, h1.w, a);
-              acc[t] = a;
+              acc[u][t] = a;
             }
           }
         }
-        bool on = false;
 #pragma unroll
-        for (int t = 0; t < NB; ++t) {
-          float s = acc[t];
-          for (int o = GL >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (valid) on |= (s + Ld.c_p[s0 + rl]) > 0.f;
+        for (int u = 0; u < RU; ++u) {
+          const int rl = ((it0 + u) * kWarps + wid) * rows_per_warp + lane / GL;
+          const bool valid = it0 + u < iters && rl < n_rows;
+          bool on = false;
+#pragma unroll
+          for (int t = 0; t < NB; ++t) {
+            float s = acc[u][t];
+            for (int o = GL >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (valid) on |= (s + Ld.c_p[s0 + rl]) > 0.f;
+          }
+          if (valid && sub == 0) flag_s[rl] = on ? 1 : 0;
         }
-        if (valid && sub == 0) flag_s[rl] = on ? 1 : 0;
       }
     }
     __syncthreads();
+    PHASE_STAMP(l, 4);
     // ordered compaction of flag_s[0 .. s1-s0)
     {
       const int n_rows = s1 - s0;
@@ -231,14 +266,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
       }
     }
+    PHASE_STAMP(l, 5);
     if (!grid_barrier(p.bar, ++epoch, status)) return;
+    PHASE_STAMP(l, 6);
 
     // ---------------- E: my chunk of the global list, up + down
     if (tid < 32) {
-      // exclusive prefix of the G local counts (one warp)
+      // exclusive prefix of the G local counts (one warp; all loads issued first)
+      constexpr int kCntRegs = 8;
+      int cv[kCntRegs];
+#pragma unroll
+      for (int q = 0; q < kCntRegs; ++q) {
+        const int c = q * 32 + lane;
+        cv[q] = c < G ? ldcg(p.cnt + c) : 0;
+      }
       int carry = 0;
       for (int c0 = 0; c0 < G; c0 += 32) {
-        const int v = c0 + lane < G ? ldcg(p.cnt + c0 + lane) : 0;
+        const int q = c0 / 32;
+        int v = 0;
+#pragma unroll
+        for (int qq = 0; qq < kCntRegs; ++qq)
+          if (qq == q) v = cv[qq];
+        if (q >= kCntRegs) v = c0 + lane < G ? ldcg(p.cnt + c0 + lane) : 0;
         int incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -269,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       chunk_s[j] = ldcg(p.lists + (size_t)lo * slice + (k - pre_s[lo]));
     }
     __syncthreads();
+    PHASE_STAMP(l, 7);
     // next layer's predictor weights: start them towards L2 now
     if (p.pf_next && l + 1 < p.n_layers) {
       const pi::LayerDev &Ln = p.layers[l + 1];
@@ -385,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       }
       __syncthreads();
     }
+    PHASE_STAMP(l, 8);
 #pragma unroll
     for (int t = 0; t < NB; ++t)
 #pragma unroll
@@ -396,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           dst[1] = make_float4(acc[t][c][4], acc[t][c][5], acc[t][c][6], acc[t][c][7]);
         }
       }
+    PHASE_STAMP(l, 9);
     if (!grid_barrier(p.bar, ++epoch, status)) return;
+    PHASE_STAMP(l, 10);
 
     // ---------------- F: y = sum of partials, columns c = cta, cta + G, ... (float4)
     {
@@ -408,10 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c < n4) {
           const float4 *pp = reinterpret_cast<const float4 *>(p.partial);
-#pragma unroll 4
-          for (int sp = g; sp < G; sp += kWarps) {
-            const float4 v = ldcg(pp + (size_t)sp * n4 + c);
-            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+          constexpr int kPR = 16;                  // split loads in flight per thread
+          for (int sp0 = g; sp0 < G; sp0 += kWarps * kPR) {
+            float4 v[kPR];
+#pragma unroll
+            for (int q = 0; q < kPR; ++q) {
+              const int sp = sp0 + q * kWarps;
+              v[q] = sp < G ? ldcg(pp + (size_t)sp * n4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < kPR; ++q) {
+              s.x += v[q].x; s.y += v[q].y; s.z += v[q].z; s.w += v[q].w;
+            }
           }
         }
         fred_s[g][col_l] = s;
@@ -427,9 +488,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         __syncthreads();
       }
     }
+    PHASE_STAMP(l, 11);
     if (!grid_barrier(p.bar, ++epoch, status)) return;
+    PHASE_STAMP(l, 12);
   }
 }
+
+#ifdef PI_PHASE_TIMING
+}  // namespace
+extern "C" int pi_debug_phase_times(unsigned long long *out) {
+  return (int)cudaMemcpyFromSymbol(out, g_phase_ts, sizeof(g_phase_ts));
+}
+namespace {
+#endif
 
 template <int CPT, int NB, bool REGLU>
 cudaError_t launch_step(const pi::StackParams &p, size_t smem, cudaStream_t s) {

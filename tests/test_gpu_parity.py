@@ -121,9 +121,10 @@ def test_rows_outside_set_are_never_read(pi, act):
     t, L = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1), seed=19)
     x = make_tokens(d, 1, seed=23).cuda()
     clean = pi.Layer.from_dict(to_dev(t))
-    y0, idx, count = clean.forward(x)
+    _, idx, count = clean.forward(x)
     torch.cuda.synchronize()
     S = idx[:int(count.item())].cpu().numpy()
+    y0 = clean.sparse_ffn(x, torch.from_numpy(S.astype(np.int32)).cuda(), count)
     out = torch.from_numpy(np.setdiff1d(np.arange(ffn), S))
     p = dict(t)
     p["W_up"] = t["W_up"].clone(); p["W_up"][out] = float("nan")
