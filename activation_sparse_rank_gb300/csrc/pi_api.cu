@@ -173,11 +173,10 @@ WsLayout ws_layout(const pi_layer *L, int B) {
   w.h = off;       off += align_up(sizeof(float) * (size_t)B * L->rank);
   w.a = off;       off += align_up(sizeof(float) * (size_t)B * L->ffn);
   w.partial = off; off += align_up(sizeof(float) * (size_t)nsplit * B * L->d);
-  w.mask = off;    off += align_up((size_t)B * L->ffn);
+  w.mask = off;    off += align_up((size_t)std::max(B, kMaxStack) * L->ffn);
   w.idx = off;     off += align_up(sizeof(int32_t) * (size_t)L->ffn);
   w.count = off;   off += align_up(sizeof(int32_t) * 4);
   w.cnt = off;     off += align_up(sizeof(int32_t) * (size_t)step_grid(L));
-  w.lists = off;   off += align_up(sizeof(int32_t) * (size_t)step_grid(L) * step_slice(L));
   w.bar = off;     off += align_up(sizeof(unsigned));
   w.total = off;
   return w;
@@ -252,7 +251,6 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   pi_layer *L = new (std::nothrow) pi_layer();
   if (!L) return pi::fail(PI_ERR_OOM, "host allocation failed");
   L->d = d; L->ffn = ffn; L->rank = r; L->act = D->act;
-  L->perm = std::move(p);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto bail = [&](pi_status code) {
     if (L->base) cudaFree(L->base);
@@ -262,6 +260,18 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   if (cudaGetDevice(&L->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device) != cudaSuccess)
     return bail(pi::fail(PI_ERR_CUDA, "no usable CUDA device"));
+  // Deal the caller's order round-robin over the G SM slices of the persistent
+  // step: the k-th neuron of `p` goes to slice k % G, place k / G within it.
+  // Each slice then holds every G-th neuron of a hot-first order, the same mix
+  // of hot and cold neurons.
+  {
+    const int G = pi::step_grid(L), q = ffn / G, rr = ffn % G;
+    L->perm.resize(ffn);
+    for (int k = 0; k < ffn; ++k) {
+      const int c = k % G, j = k / G;
+      L->perm[(size_t)c * q + std::min(c, rr) + j] = p[k];
+    }
+  }
 
   const size_t wrow = (size_t)ffn * d * sizeof(__half);
   size_t off = 0;
@@ -467,6 +477,7 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
   if (!y || !aligned16(y)) return pi::fail(PI_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
   if ((idx && !aligned4(idx)) || (count && !aligned4(count)))
     return pi::fail(PI_ERR_INVALID_ARG, "idx and count must be 4-byte aligned");
+  if (idx && !count) return pi::fail(PI_ERR_INVALID_ARG, "an idx output needs a count output");
   if (B > 2 && (!idx || !count))
     return pi::fail(PI_ERR_INVALID_ARG, "B > 2 needs idx and count buffers");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -49,11 +49,10 @@ struct WsLayout {
   size_t h = 0;        // float [B, rank]
   size_t a = 0;        // float [B, ffn]        activations by list position
   size_t partial = 0;  // float [nsplit, B, d]  split-K partial sums
-  size_t mask = 0;     // uint8 [B, ffn]
+  size_t mask = 0;     // uint8 [max(B, kMaxStack), ffn]
   size_t idx = 0;      // int32 [ffn]           (pi_layer_forward when idx not given)
   size_t count = 0;    // int32 [4]
   size_t cnt = 0;      // int32 [G]             per-CTA active counts (persistent step)
-  size_t lists = 0;    // int32 [G, slice]      per-CTA local active lists
   size_t bar = 0;      // uint32                grid-barrier counter
   size_t total = 0;
 };
@@ -70,14 +69,14 @@ struct LayerDev {
 // Kernel parameters of the persistent step (passed by value, < 4 KB).
 struct StackParams {
   int n_layers, d, ffn, rank;
-  int G, slice, lanes_l, sub, pf_rows, pf_next;
+  int G, staged, lanes_l, pf_rows, pf_next;
+  int off_flag, off_list, off_p1, off_p2;   // dynamic shared memory offsets
   const __half *x;       // [n_layers, B, d]
   float *y;              // [n_layers, B, d]
-  int32_t *idx;          // [n_layers, ffn] or nullptr
   int32_t *count;        // [n_layers] or nullptr
+  uint8_t *mask_out;     // [n_layers, ffn] union masks (for the idx output) or nullptr
   float *h;              // scratch [B, rank]
   int32_t *cnt;          // scratch [G]
-  int32_t *lists;        // scratch [G, slice]
   float *partial;        // scratch [G, B, d]
   unsigned *bar;         // scratch barrier counter (zeroed before launch)
   unsigned *status;
@@ -85,7 +84,11 @@ struct StackParams {
 };
 int step_grid(const pi_layer *L);
 int step_slice(const pi_layer *L);
+bool step_staged(const pi_layer *L, int B);
 size_t step_smem(const pi_layer *L, int B);
+// Ascending active lists of n layers from their union masks [n, ffn] (one CTA per layer).
+cudaError_t run_compact_layers(const pi_layer *L, const uint8_t *masks, int n, int32_t *idx,
+                               int32_t *count, cudaStream_t s);
 cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, int32_t *idx,
                       int32_t *count, float *y, const WsLayout &w, char *ws, cudaStream_t s);
 WsLayout ws_layout(const pi_layer *L, int B);

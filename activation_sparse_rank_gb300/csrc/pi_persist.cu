@@ -5,31 +5,33 @@
 // (egguo-blog reading report), section 2.3, core modules 3 (predictor) and 4
 // (neuron-aware operators), run layer after layer for one decode batch.
 //
-// One CTA per SM.  Per layer, four grid-wide phases separated by barriers:
+// One CTA per SM.  The layer's neurons are stored hot-first and dealt
+// round-robin over the G SM slices (see pi_layer_create), so every CTA's
+// contiguous slice holds the same mix of hot and cold neurons and a similar
+// expected number of active ones.  Per layer, three grid-wide barriers:
 //   A  h = ReLU(W_p1 x): predictor rows k = cta, cta+G, ... (whole CTA per row)
-//   C  l = W_p2 h + c_p over the CTA's contiguous neuron slice, threshold,
-//      ordered local active list; the CTA immediately asks L2 to stream in the
-//      up/gate/down rows of its own active neurons, so HBM traffic for the
-//      sparse FFN starts before the global list exists
-//   E  global list = concatenation of the local lists (prefix of their
-//      counts); CTA j takes the j-th equal chunk of it, forms a and its
-//      partial y (rows stream through L2 in windows), and meanwhile prefetches
-//      the next layer's predictor weights into L2
-//   F  y = sum of the partials in fixed split order (deterministic)
-// A barrier follows F so the next layer may depend on y, as in real decode.
+//   -- barrier 1 (h complete)
+//   C  l = W_p2 h + c_p over the CTA's slice, threshold, ordered local list
+//   E  the CTA streams the up/gate/down rows of its own active neurons (bulk
+//      L2 prefetch of all of them first, then 16-byte loads in windows), forms
+//      a and its partial y; meanwhile the next layer's predictor weights are
+//      staged into shared memory by TMA (or prefetched into L2 when too big)
+//   -- barrier 2 (partials complete)
+//   F  y = sum of the G partials in a fixed order (deterministic)
+//   -- barrier 3 (y complete: the next layer may depend on it, as in decode)
 //
-// Grid barriers spin on a global counter with an iteration cap; on timeout a
-// status bit is set and every CTA returns (no trap, no unbounded wait).  Data
-// written inside the kernel (h, counts, lists, partials) is read with
-// ld.global.cg (L2, coherent); only weights and x use the read-only path.
+// Grid barriers are a release-add on a global counter and an acquire poll
+// with an iteration cap; mbarrier waits are capped too.  On a cap the kernel
+// sets a status bit and returns (no trap, no unbounded wait).  Data written
+// inside the kernel (h, counts, partials) is read with ld.global.cg (L2,
+// coherent); only weights and x use the read-only path.
 #include "pi_internal.cuh"
 
 namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kWin = 32;               // max neurons per phase-E window
-constexpr unsigned kSpinLimit = 1u << 22;   // ~seconds of polling, then give up
+constexpr unsigned kSpinLimit = 1u << 22;   // polls before a wait gives up (seconds)
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
   unsigned v;
@@ -40,37 +42,59 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 template <typename T>
 __device__ __forceinline__ T ldcg(const T *p) { return __ldcg(p); }
 
-// Grid barrier number `epoch` (1, 2, ...).  Returns false (after setting the
-// timeout bit) if the other CTAs did not arrive within the spin cap or an
-// error was already flagged.
+// Grid barrier number `epoch` (1, 2, ...).  False if the wait ran out (status set).
 __device__ bool grid_barrier(unsigned *bar, unsigned epoch, unsigned *status) {
   __shared__ int ok_s;
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned target = epoch * gridDim.x;
-    __threadfence();
-    atomicAdd(bar, 1u);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
     int ok = 1;
     unsigned it = 0;
-    while (true) {
-      const unsigned v = ld_acquire(bar);
-      if ((int)(v - target) >= 0) break;
+    while ((int)(ld_acquire(bar) - target) < 0) {
       if (++it > kSpinLimit) {
         atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
         ok = 0;
         break;
       }
     }
-    __threadfence();
     ok_s = ok;
   }
   __syncthreads();
   return ok_s != 0;
 }
 
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Bounded wait for mbarrier phase `parity`.  False if it ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+  for (unsigned it = 0; it < kSpinLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_1d(void *dst_smem, const void *src, uint32_t bytes,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
 #ifdef PI_PHASE_TIMING
-// Diagnostic build only: globaltimer stamps at phase boundaries of CTA 0 and
-// CTA G-1 for the first 16 layers of the most recent launch.
+// Diagnostic build only: globaltimer stamps at phase boundaries of three CTAs
+// for the first 16 layers of the most recent launch.
 __device__ unsigned long long g_phase_ts[3][16][16];
 #define PHASE_STAMP(l, ph)                                                        \
   do {                                                                            \
@@ -85,37 +109,71 @@ __device__ unsigned long long g_phase_ts[3][16][16];
 #define PHASE_STAMP(l, ph) do {} while (0)
 #endif
 
+// Issue the predictor weights of layer Ld for this CTA into shared memory
+// (one thread): its W_p1 rows k = cta, cta+G, ... and its W_p2 slice.
+__device__ __forceinline__ void stage_predictor(const pi::LayerDev &Ld, int cta, int G, int d, int r,
+                                                int s0, int s1, __half *p1_s, __half *p2_s,
+                                                uint32_t mbar) {
+  int na = 0;
+  for (int k = cta; k < r; k += G) ++na;
+  const uint32_t row_bytes = (uint32_t)d * 2u;
+  const uint32_t p2_bytes = (uint32_t)(s1 - s0) * (uint32_t)r * 2u;
+  const uint32_t total = (uint32_t)na * row_bytes + p2_bytes;
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(total) : "memory");
+  int q = 0;
+  for (int k = cta; k < r; k += G, ++q)
+    tma_load_1d(p1_s + (size_t)q * d, Ld.W_p1 + (size_t)k * d, row_bytes, mbar);
+  if (p2_bytes) tma_load_1d(p2_s, Ld.W_p2 + (size_t)s0 * r, p2_bytes, mbar);
+}
+
 template <int CPT, int NB, bool REGLU>
 __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constant__ pi::StackParams p) {
-  constexpr int G1 = CPT == 1 ? 16 : 8 / CPT > 0 ? 8 / CPT : 1;     // phase-E loads per group
-  constexpr int GU = (REGLU ? G1 / 2 : G1) > 0 ? (REGLU ? G1 / 2 : G1) : 1;
-  constexpr int NR = REGLU ? 2 : 1;
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ float red_s[kWarps][NB][NR][kWin];
-  __shared__ float a_s[NB][kWin];
-  __shared__ int win_s[2][kWin];
-  __shared__ float4 fred_s[16][32];
+  constexpr int NR = REGLU ? 2 : 1;                          // gated rows per neuron
+  constexpr int LOADS = CPT == 1 ? 24 : 16;                  // 16-byte loads in flight per thread
+  constexpr int GW0 = LOADS / (CPT * (NR + 1));
+  constexpr int GW = GW0 > 0 ? GW0 : 1;                      // neurons per phase-E window
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float red_s[kWarps][NB][NR][GW];
+  __shared__ float a_s[NB][GW];
+  __shared__ float ared_s[kWarps][NB][8];
+  __shared__ float4 fred_s[2][8];
+  __shared__ int wtot_s[kWarps];
+  __shared__ __align__(8) unsigned long long mbar_s;
 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
   const int d = p.d, ffn = p.ffn, r = p.rank, nv = d >> 3;
-  const int slice = p.slice;
   const uint32_t row_bytes = (uint32_t)d * 2u;
   unsigned *status = p.status;
   unsigned epoch = 0;
+  const uint32_t mbar = smem_u32(&mbar_s);
 
-  // dynamic shared memory carve-up
-  float *h_s = reinterpret_cast<float *>(smem);                         // [NB, r]
-  int *pre_s = reinterpret_cast<int *>(h_s + NB * r);                   // [G + 1]
-  int *list_s = pre_s + ((G + 1 + 3) & ~3);                             // [slice]
-  int *chunk_s = list_s + slice;                                        // [slice]
-  unsigned char *flag_s = reinterpret_cast<unsigned char *>(chunk_s + slice);   // [slice]
+  // this CTA's neuron slice [s0, s1): sizes differ by at most one
+  const int q_sl = ffn / G, r_sl = ffn % G;
+  const int s0 = cta * q_sl + min(cta, r_sl);
+  const int s1 = s0 + q_sl + (cta < r_sl ? 1 : 0);
+  const int n_rows = s1 - s0;
 
-  const int s0 = min(ffn, cta * slice), s1 = min(ffn, s0 + slice);     // my predictor slice
+  // dynamic shared memory carve-up (sizes from pi::step_smem)
+  float *h_s = reinterpret_cast<float *>(smem);                                     // [NB, r]
+  unsigned char *flag_s = reinterpret_cast<unsigned char *>(smem) + p.off_flag;    // [slice]
+  int *list_s = reinterpret_cast<int *>(smem + p.off_list);                        // [slice]
+  __half *p1_s = reinterpret_cast<__half *>(smem + p.off_p1);                      // [na_max, d]
+  __half *p2_s = reinterpret_cast<__half *>(smem + p.off_p2);                      // [slice, r]
+
+  if (p.staged) {
+    if (tid == 0) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar));
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0) stage_predictor(p.layers[0], cta, G, d, r, s0, s1, p1_s, p2_s, mbar);
+  }
 
   for (int l = 0; l < p.n_layers; ++l) {
     const pi::LayerDev &Ld = p.layers[l];
     const __half *x = p.x + (size_t)l * NB * d;
+    PHASE_STAMP(l, 0);
 
     uint4 xr[NB][CPT];
 #pragma unroll
@@ -127,38 +185,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
                           : make_uint4(0, 0, 0, 0);
       }
 
-    PHASE_STAMP(l, 0);
-    // ---------------- A: h = ReLU(W_p1 x), rows cta, cta + G, ...
-    for (int k0 = cta; k0 < r; k0 += 2 * G) {
-      uint4 w[2][CPT];
+    if (p.staged && !mbar_wait(mbar, (uint32_t)(l & 1))) {
+      if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
+      mbar_wait(mbar, (uint32_t)(l & 1));     // let a copy still in flight land
+      return;
+    }
+
+    // ---------------- A: h = ReLU(W_p1 x), rows cta, cta + G, ... (8 rows per pass)
+    for (int q0 = 0; cta + q0 * G < r; q0 += 8) {
+      float hs[8][NB];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int k = k0 + q * G;
+      for (int q = 0; q < 8; ++q) {
+        const int k = cta + (q0 + q) * G;
+        uint4 w[CPT];
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
           const int v = tid + c * kThreads;
-          w[q][c] = (k < r && v < nv)
-                        ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p1 + (size_t)k * d) + v)
-                        : make_uint4(0, 0, 0, 0);
+          if (k < r && v < nv)
+            w[c] = p.staged ? reinterpret_cast<const uint4 *>(p1_s + (size_t)(q0 + q) * d)[v]
+                            : pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p1 + (size_t)k * d) + v);
+          else
+            w[c] = make_uint4(0, 0, 0, 0);
         }
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
           float s = 0.f;
 #pragma unroll
-          for (int c = 0; c < CPT; ++c) s = pidev::dot8(s, w[q][c], xr[t][c]);
-          s = pidev::warp_sum(s);
-          if (lane == 0) red_s[wid][t][0][q] = s;
+          for (int c = 0; c < CPT; ++c) s = pidev::dot8(s, w[c], xr[t][c]);
+          hs[q][t] = s;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int t = 0; t < NB; ++t) {
+          const float s = pidev::warp_sum(hs[q][t]);
+          if (lane == 0) ared_s[wid][t][q] = s;
         }
       __syncthreads();
-      if (tid < 2 * NB) {
+      if (tid < 8 * NB) {
         const int q = tid / NB, t = tid % NB;
-        const int k = k0 + q * G;
+        const int k = cta + (q0 + q) * G;
         if (k < r) {
           float s = 0.f;
-          for (int w2 = 0; w2 < kWarps; ++w2) s += red_s[w2][t][0][q];
+          for (int w2 = 0; w2 < kWarps; ++w2) s += ared_s[w2][t][q];
           p.h[(size_t)t * r + k] = s > 0.f ? s : 0.f;
         }
       }
@@ -168,16 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     if (!grid_barrier(p.bar, ++epoch, status)) return;
     PHASE_STAMP(l, 2);
 
-    // ---------------- C: logits over my slice, local ordered active list
+    // ---------------- C: logits over my slice, ordered local active list
     for (int e = tid; e < NB * r; e += kThreads) h_s[e] = ldcg(p.h + e);
     __syncthreads();
-    PHASE_STAMP(l, 3);
     {
       const int GL = p.lanes_l;                 // lanes per predictor row (8, 16, 32)
       const int rows_per_warp = 32 / GL;
       const int sub = lane % GL;
       const int nvr = r >> 3;
-      const int n_rows = s1 - s0;
       const int iters = (n_rows + kWarps * rows_per_warp - 1) / (kWarps * rows_per_warp);
       constexpr int RU = 8;                     // rows in flight per lane
       for (int it0 = 0; it0 < iters; it0 += RU) {
@@ -191,9 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
 #pragma unroll
           for (int u = 0; u < RU; ++u) {
             const int rl = ((it0 + u) * kWarps + wid) * rows_per_warp + lane / GL;
-            wv[u] = (it0 + u < iters && rl < n_rows)
-                        ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p2 + (size_t)(s0 + rl) * r) + v)
-                        : make_uint4(0, 0, 0, 0);
+            if (it0 + u < iters && rl < n_rows)
+              wv[u] = p.staged ? reinterpret_cast<const uint4 *>(p2_s + (size_t)rl * r)[v]
+                               : pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p2 + (size_t)(s0 + rl) * r) + v);
+            else
+              wv[u] = make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int t = 0; t < NB; ++t) {
@@ -229,16 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       }
     }
     __syncthreads();
-    PHASE_STAMP(l, 4);
-    // ordered compaction of flag_s[0 .. s1-s0)
+    int lcount = 0;
     {
-      const int n_rows = s1 - s0;
-      int base = 0;
       for (int c0 = 0; c0 < n_rows; c0 += kThreads) {
         const int i = c0 + tid;
         const bool on = i < n_rows && flag_s[i];
         const unsigned bal = __ballot_sync(0xffffffffu, on);
-        __shared__ int wtot_s[kWarps];
         if (lane == 0) wtot_s[wid] = __popc(bal);
         __syncthreads();
         int wpre = 0, tot = 0;
@@ -247,17 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           if (q < wid) wpre += v;
           tot += v;
         }
-        if (on) {
-          const int pos = base + wpre + __popc(bal & ((1u << lane) - 1u));
-          list_s[pos] = s0 + i;
-        }
-        base += tot;
+        if (on) list_s[lcount + wpre + __popc(bal & ((1u << lane) - 1u))] = s0 + i;
+        lcount += tot;
         __syncthreads();
       }
-      const int lcount = base;
-      for (int j = tid; j < lcount; j += kThreads) p.lists[(size_t)cta * slice + j] = list_s[j];
+      if (p.mask_out)
+        for (int i = tid; i < n_rows; i += kThreads) p.mask_out[(size_t)l * ffn + s0 + i] = flag_s[i];
       if (tid == 0) p.cnt[cta] = lcount;
-      // stream my own active rows towards L2 now (bounded by the prefetch budget)
+      // ask L2 for all my active rows now (bounded by the prefetch budget)
       const int npf = min(lcount, p.pf_rows);
       for (int j = tid; j < npf; j += kThreads) {
         const int i = list_s[j];
@@ -266,73 +329,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
       }
     }
-    PHASE_STAMP(l, 5);
-    if (!grid_barrier(p.bar, ++epoch, status)) return;
-    PHASE_STAMP(l, 6);
+    PHASE_STAMP(l, 3);
 
-    // ---------------- E: my chunk of the global list, up + down
-    if (tid < 32) {
-      // exclusive prefix of the G local counts (one warp; all loads issued first)
-      constexpr int kCntRegs = 8;
-      int cv[kCntRegs];
-#pragma unroll
-      for (int q = 0; q < kCntRegs; ++q) {
-        const int c = q * 32 + lane;
-        cv[q] = c < G ? ldcg(p.cnt + c) : 0;
-      }
-      int carry = 0;
-      for (int c0 = 0; c0 < G; c0 += 32) {
-        const int q = c0 / 32;
-        int v = 0;
-#pragma unroll
-        for (int qq = 0; qq < kCntRegs; ++qq)
-          if (qq == q) v = cv[qq];
-        if (q >= kCntRegs) v = c0 + lane < G ? ldcg(p.cnt + c0 + lane) : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        if (c0 + lane < G) pre_s[c0 + lane] = carry + incl - v;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) pre_s[G] = carry;
-    }
-    __syncthreads();
-    const int total = pre_s[G];
-    if (cta == 0 && tid == 0 && p.count) p.count[l] = total;
-    if (p.idx) {
-      const int my0 = pre_s[cta], myn = pre_s[cta + 1] - my0;
-      for (int j = tid; j < myn; j += kThreads) p.idx[(size_t)l * ffn + my0 + j] = list_s[j];
-    }
-    const int chunk = (total + G - 1) / G;
-    const int k0 = min(total, cta * chunk), k1 = min(total, k0 + chunk);
-    for (int j = tid; j < k1 - k0; j += kThreads) {
-      const int k = k0 + j;
-      int lo = 0, hi = G - 1;                 // largest o with pre_s[o] <= k
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre_s[mid] <= k) lo = mid; else hi = mid - 1;
-      }
-      chunk_s[j] = ldcg(p.lists + (size_t)lo * slice + (k - pre_s[lo]));
-    }
-    __syncthreads();
-    PHASE_STAMP(l, 7);
-    // next layer's predictor weights: start them towards L2 now
-    if (p.pf_next && l + 1 < p.n_layers) {
+    // next layer's predictor weights: TMA into shared memory, or L2 prefetch
+    if (l + 1 < p.n_layers && tid == 0) {
       const pi::LayerDev &Ln = p.layers[l + 1];
-      if (tid == 0)
+      if (p.staged) {
+        stage_predictor(Ln, cta, G, d, r, s0, s1, p1_s, p2_s, mbar);
+      } else if (p.pf_next) {
         for (int k = cta; k < r; k += G) pidev::prefetch_l2_bulk(Ln.W_p1 + (size_t)k * d, row_bytes);
-      const uint32_t p2_bytes = (uint32_t)(s1 - s0) * (uint32_t)r * 2u;
-      if (tid == 1 && s1 > s0) {
-        // bulk prefetch sizes are limited; split into 64 KB pieces
+        const uint32_t p2_bytes = (uint32_t)n_rows * (uint32_t)r * 2u;
         const char *base = reinterpret_cast<const char *>(Ln.W_p2 + (size_t)s0 * r);
         for (uint32_t o = 0; o < p2_bytes; o += 65536u)
           pidev::prefetch_l2_bulk(base + o, min(65536u, p2_bytes - o));
       }
     }
 
+    // ---------------- E: up (+gate) and down rows of my active neurons
     float acc[NB][CPT][8];
 #pragma unroll
     for (int t = 0; t < NB; ++t)
@@ -341,101 +354,77 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[t][c][e] = 0.f;
 
-    const int n_chunk = k1 - k0;
-    const int win = p.sub;
-    auto prefetch_window = [&](int w0, int buf) {
-      const int w1 = min(n_chunk, w0 + win);
-      for (int j = w0 + tid; j < w1; j += kThreads) {
-        const int i = chunk_s[j];
-        win_s[buf][j - w0] = i;
-        pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
-        if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
-        pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+    for (int w0 = 0; w0 < lcount; w0 += GW) {
+      const int n_here = min(GW, lcount - w0);
+      if (w0 + GW > p.pf_rows)                  // rows past the early-prefetch budget
+        for (int j = max(w0, p.pf_rows) + tid; j < w0 + n_here; j += kThreads) {
+          const int i = list_s[j];
+          pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
+          if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
+          pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+        }
+      uint4 wu[GW][NR][CPT], wd[GW][CPT];
+#pragma unroll
+      for (int n = 0; n < GW; ++n) {
+        const int i = n < n_here ? list_s[w0 + n] : -1;
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          const int v = tid + c * kThreads;
+          const bool ok = i >= 0 && v < nv;
+          wu[n][0][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_up + (size_t)i * d) + v)
+                           : make_uint4(0, 0, 0, 0);
+          if (REGLU)
+            wu[n][NR - 1][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_gate + (size_t)i * d) + v)
+                                  : make_uint4(0, 0, 0, 0);
+          wd[n][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_dT + (size_t)i * d) + v)
+                        : make_uint4(0, 0, 0, 0);
+        }
       }
-    };
-    if (n_chunk > 0) prefetch_window(0, 0);
-    __syncthreads();
-    int buf = 0;
-    for (int w0 = 0; w0 < n_chunk; w0 += win, buf ^= 1) {
-      const int n_here = min(win, n_chunk - w0);
-      if (w0 + win < n_chunk) prefetch_window(w0 + win, buf ^ 1);
-      for (int g0 = 0; g0 < n_here; g0 += GU) {
-        uint4 w[GU][NR][CPT];
 #pragma unroll
-        for (int n = 0; n < GU; ++n) {
-          const int i = g0 + n < n_here ? win_s[buf][g0 + n] : -1;
+      for (int n = 0; n < GW; ++n)
 #pragma unroll
-          for (int c = 0; c < CPT; ++c) {
-            const int v = tid + c * kThreads;
-            const bool ok = i >= 0 && v < nv;
-            w[n][0][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_up + (size_t)i * d) + v)
-                            : make_uint4(0, 0, 0, 0);
-            if (REGLU)
-              w[n][NR - 1][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_gate + (size_t)i * d) + v)
-                                   : make_uint4(0, 0, 0, 0);
+        for (int q = 0; q < NR; ++q)
+#pragma unroll
+          for (int t = 0; t < NB; ++t) {
+            float s = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) s = pidev::dot8(s, wu[n][q][c], xr[t][c]);
+            s = pidev::warp_sum(s);
+            if (lane == 0) red_s[wid][t][q][n] = s;
           }
-        }
-#pragma unroll
-        for (int n = 0; n < GU; ++n)
-#pragma unroll
-          for (int q = 0; q < NR; ++q)
-#pragma unroll
-            for (int t = 0; t < NB; ++t) {
-              float s = 0.f;
-#pragma unroll
-              for (int c = 0; c < CPT; ++c) s = pidev::dot8(s, w[n][q][c], xr[t][c]);
-              s = pidev::warp_sum(s);
-              if (lane == 0 && g0 + n < n_here) red_s[wid][t][q][g0 + n] = s;
-            }
-      }
       __syncthreads();
-      for (int e = tid; e < NB * n_here; e += kThreads) {
-        const int t = e / n_here, n = e % n_here;
-        const int i = win_s[buf][n];
-        float su = 0.f, sg = 0.f;
-        for (int q = 0; q < kWarps; ++q) {
-          su += red_s[q][t][0][n];
-          if (REGLU) sg += red_s[q][t][NR - 1][n];
-        }
-        float a;
-        if (REGLU) {
-          const float gz = sg + Ld.b[i];
-          a = (gz > 0.f ? gz : 0.f) * su;
-        } else {
-          const float z = su + Ld.b[i];
-          a = z > 0.f ? z : 0.f;
+      if (tid < NB * GW) {
+        const int t = tid / GW, n = tid % GW;
+        float a = 0.f;
+        if (n < n_here) {
+          const int i = list_s[w0 + n];
+          float su = 0.f, sg = 0.f;
+          for (int q = 0; q < kWarps; ++q) {   // fixed order over warps
+            su += red_s[q][t][0][n];
+            if (REGLU) sg += red_s[q][t][NR - 1][n];
+          }
+          if (REGLU) {
+            const float gz = sg + Ld.b[i];
+            a = (gz > 0.f ? gz : 0.f) * su;
+          } else {
+            const float z = su + Ld.b[i];
+            a = z > 0.f ? z : 0.f;
+          }
         }
         a_s[t][n] = a;
       }
       __syncthreads();
-      for (int g0 = 0; g0 < n_here; g0 += G1) {
-        uint4 w[G1][CPT];
 #pragma unroll
-        for (int n = 0; n < G1; ++n) {
-          const int i = g0 + n < n_here ? win_s[buf][g0 + n] : -1;
+      for (int n = 0; n < GW; ++n)
 #pragma unroll
-          for (int c = 0; c < CPT; ++c) {
-            const int v = tid + c * kThreads;
-            w[n][c] = (i >= 0 && v < nv)
-                          ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_dT + (size_t)i * d) + v)
-                          : make_uint4(0, 0, 0, 0);
-          }
+        for (int t = 0; t < NB; ++t) {
+          const float an = a_s[t][n];
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) pidev::axpy8(acc[t][c], an, wd[n][c]);
         }
-#pragma unroll
-        for (int n = 0; n < G1; ++n) {
-          if (g0 + n < n_here) {
-#pragma unroll
-            for (int t = 0; t < NB; ++t) {
-              const float an = a_s[t][g0 + n];
-#pragma unroll
-              for (int c = 0; c < CPT; ++c) pidev::axpy8(acc[t][c], an, w[n][c]);
-            }
-          }
-        }
-      }
-      __syncthreads();
+      __syncthreads();   // red_s / a_s are rewritten by the next window
     }
-    PHASE_STAMP(l, 8);
+    PHASE_STAMP(l, 4);
 #pragma unroll
     for (int t = 0; t < NB; ++t)
 #pragma unroll
@@ -447,26 +436,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           dst[1] = make_float4(acc[t][c][4], acc[t][c][5], acc[t][c][6], acc[t][c][7]);
         }
       }
-    PHASE_STAMP(l, 9);
+    PHASE_STAMP(l, 5);
     if (!grid_barrier(p.bar, ++epoch, status)) return;
-    PHASE_STAMP(l, 10);
+    PHASE_STAMP(l, 6);
 
-    // ---------------- F: y = sum of partials, columns c = cta, cta + G, ... (float4)
+    // ---------------- F: y = sum of partials.  Columns (float4) c = cta*8 + j
+    // (+ G*8 per pass); thread (j, g): j = tid / 64 column, g = tid % 64 split
+    // group summing splits g, g+64, ... in order; then a fixed shuffle tree
+    // over the 32 lanes of each warp, and the two warps of a column in order.
+    if (cta == 0 && p.count && wid == 0) {
+      int s = 0;
+      for (int c = lane; c < G; c += 32) s += ldcg(p.cnt + c);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) p.count[l] = s;
+    }
     {
       const int n4 = NB * d / 4;
-      const int col_l = tid & 31, g = tid >> 5;     // 32 columns x 16 split groups per pass
+      const int j = tid >> 6, g = tid & 63;
       float *y = p.y + (size_t)l * NB * d;
-      for (int c0 = cta * 32; c0 < n4; c0 += G * 32) {
-        const int c = c0 + col_l;
+      const float4 *pp = reinterpret_cast<const float4 *>(p.partial);
+      for (int c0 = cta * 8; c0 < n4; c0 += G * 8) {
+        const int c = c0 + j;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c < n4) {
-          const float4 *pp = reinterpret_cast<const float4 *>(p.partial);
-          constexpr int kPR = 16;                  // split loads in flight per thread
-          for (int sp0 = g; sp0 < G; sp0 += kWarps * kPR) {
+          constexpr int kPR = 8;
+          for (int sp0 = g; sp0 < G; sp0 += 64 * kPR) {
             float4 v[kPR];
 #pragma unroll
             for (int q = 0; q < kPR; ++q) {
-              const int sp = sp0 + q * kWarps;
+              const int sp = sp0 + q * 64;
               v[q] = sp < G ? ldcg(pp + (size_t)sp * n4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
@@ -475,22 +474,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
             }
           }
         }
-        fred_s[g][col_l] = s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+          s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+          s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+          s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+        }
+        if (lane == 0) fred_s[(tid >> 5) & 1][j] = s;
         __syncthreads();
         if (g == 0 && c < n4) {
-          float4 t4 = fred_s[0][col_l];
-          for (int q = 1; q < kWarps; ++q) {
-            const float4 v = fred_s[q][col_l];
-            t4.x += v.x; t4.y += v.y; t4.z += v.z; t4.w += v.w;
-          }
-          reinterpret_cast<float4 *>(y)[c] = t4;
+          const float4 a0 = fred_s[0][j], a1 = fred_s[1][j];
+          reinterpret_cast<float4 *>(y)[c] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
         }
         __syncthreads();
       }
     }
-    PHASE_STAMP(l, 11);
+    PHASE_STAMP(l, 7);
     if (!grid_barrier(p.bar, ++epoch, status)) return;
-    PHASE_STAMP(l, 12);
+    PHASE_STAMP(l, 8);
   }
 }
 
@@ -536,6 +538,29 @@ cudaError_t dispatch_step(const pi::StackParams &p, size_t smem, cudaStream_t s)
   }
 }
 
+constexpr size_t kSmemBudget = 200 * 1024;   // dynamic shared memory the step may use
+
+size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
+
+struct SmemPlan {
+  size_t off_flag, off_list, off_p1, off_p2, base_end, staged_end;
+};
+
+SmemPlan smem_plan(const pi_layer *L, int B) {
+  const int G = pi::step_grid(L);
+  const size_t slice = (size_t)pi::step_slice(L);
+  const size_t na_max = (size_t)(L->rank + G - 1) / G;
+  SmemPlan s;
+  size_t off = align128(sizeof(float) * (size_t)B * L->rank);
+  s.off_flag = off;  off = align128(off + slice);
+  s.off_list = off;  off = align128(off + sizeof(int) * slice);
+  s.base_end = off;
+  s.off_p1 = off;    off = align128(off + na_max * L->d * 2);
+  s.off_p2 = off;    off = align128(off + slice * L->rank * 2);
+  s.staged_end = off;
+  return s;
+}
+
 }  // namespace
 
 namespace pi {
@@ -544,43 +569,43 @@ int step_grid(const pi_layer *L) { return L->num_sms; }
 
 int step_slice(const pi_layer *L) { return (L->ffn + step_grid(L) - 1) / step_grid(L); }
 
+bool step_staged(const pi_layer *L, int B) { return smem_plan(L, B).staged_end <= kSmemBudget; }
+
 size_t step_smem(const pi_layer *L, int B) {
-  const int G = step_grid(L), slice = step_slice(L);
-  size_t b = sizeof(float) * (size_t)B * L->rank;
-  b += sizeof(int) * (size_t)((G + 1 + 3) & ~3);
-  b += sizeof(int) * 2 * (size_t)slice + (size_t)slice;
-  return (b + 15) & ~(size_t)15;
+  const SmemPlan s = smem_plan(L, B);
+  return s.staged_end <= kSmemBudget ? s.staged_end : s.base_end;
 }
 
 cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, int32_t *idx,
                       int32_t *count, float *y, const WsLayout &w, char *ws, cudaStream_t s) {
   const pi_layer *L0 = layers[0];
+  const SmemPlan sp = smem_plan(L0, B);
   StackParams p = {};
   p.n_layers = n;
   p.d = L0->d;
   p.ffn = L0->ffn;
   p.rank = L0->rank;
   p.G = step_grid(L0);
-  p.slice = step_slice(L0);
+  p.staged = step_staged(L0, B) ? 1 : 0;
+  p.off_flag = (int)sp.off_flag;
+  p.off_list = (int)sp.off_list;
+  p.off_p1 = (int)sp.off_p1;
+  p.off_p2 = (int)sp.off_p2;
   int GL = 32;
   while (GL > 8 && GL * 8 > L0->rank) GL >>= 1;
   p.lanes_l = GL;
   const int rows_per_neuron = L0->act == PI_ACT_REGLU ? 3 : 2;
-  int sub = (192 * 1024) / (2 * L0->d * rows_per_neuron);
-  p.sub = sub < 1 ? 1 : (sub > kWin ? kWin : sub);
-  // early prefetch of the local active rows: up to ~384 KB of rows per CTA
-  int pf = (384 * 1024) / (2 * L0->d * rows_per_neuron);
+  // early L2 prefetch of the local active rows: up to ~768 KB of rows per CTA
+  const int pf = (768 * 1024) / (2 * L0->d * rows_per_neuron);
   p.pf_rows = pf < 1 ? 1 : pf;
-  // next layer's predictor weights into L2 only when they are small
   const size_t pred_bytes = 2ull * L0->rank * L0->d + 2ull * L0->ffn * L0->rank;
   p.pf_next = pred_bytes <= (32ull << 20);
   p.x = x;
   p.y = y;
-  p.idx = idx;
   p.count = count;
+  p.mask_out = idx ? reinterpret_cast<uint8_t *>(ws + w.mask) : nullptr;
   p.h = reinterpret_cast<float *>(ws + w.h);
   p.cnt = reinterpret_cast<int32_t *>(ws + w.cnt);
-  p.lists = reinterpret_cast<int32_t *>(ws + w.lists);
   p.partial = reinterpret_cast<float *>(ws + w.partial);
   p.bar = reinterpret_cast<unsigned *>(ws + w.bar);
   p.status = L0->status;
@@ -599,7 +624,14 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   else
     e = reglu ? dispatch_step<2, true>(p, smem, s) : dispatch_step<2, false>(p, smem, s);
   if (e != cudaSuccess) return e;
-  return record_hook(L0->ev_after, s);
+  e = record_hook(L0->ev_after, s);
+  if (e != cudaSuccess) return e;
+  if (idx) {
+    // ascending active lists (and counts) from the per-layer masks
+    e = run_compact_layers(L0, p.mask_out, n, idx, count, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace pi

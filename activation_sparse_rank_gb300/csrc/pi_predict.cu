@@ -127,6 +127,10 @@ __global__ void __launch_bounds__(1024) k_compact(const uint8_t *__restrict__ ma
   __shared__ int warp_tot[32];
   pidev::griddep_wait();
   pidev::griddep_launch();
+  // one CTA per problem: blockIdx.x selects a [B, ffn] mask, an idx row and a count
+  mask += (size_t)blockIdx.x * B * ffn;
+  idx += (size_t)blockIdx.x * ffn;
+  count += blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int base = 0;
   for (int i0 = 0; i0 < ffn; i0 += 1024 * 16) {
@@ -216,6 +220,12 @@ cudaError_t run_compact(const pi_layer *L, const uint8_t *mask, int B, int32_t *
                         int32_t *count, cudaStream_t s) {
   const int vec = ((reinterpret_cast<uintptr_t>(mask) & 15) == 0) && (L->ffn % 16 == 0);
   return launch_pdl(k_compact, dim3(1), dim3(1024), 0, s, mask, B, L->ffn, vec, idx, count);
+}
+
+cudaError_t run_compact_layers(const pi_layer *L, const uint8_t *masks, int n, int32_t *idx,
+                               int32_t *count, cudaStream_t s) {
+  const int vec = ((reinterpret_cast<uintptr_t>(masks) & 15) == 0) && (L->ffn % 16 == 0);
+  return launch_pdl(k_compact, dim3(n), dim3(1024), 0, s, masks, 1, L->ffn, vec, idx, count);
 }
 
 }  // namespace pi

@@ -82,8 +82,14 @@ typedef struct {
 /* Build a layer object that owns a permuted, neuron-major copy of the weights
  * (section 2.3, core module 1 and variable table: neurons ordered by profiled
  * activation frequency v_i = f_i, hot first).
- *   perm  host int32 [ffn] or NULL (identity): position k of the layer holds
- *         model neuron perm[k]; must be a permutation of 0..ffn-1.
+ *   perm  host int32 [ffn] or NULL (identity): the caller's neuron order, for
+ *         example hot-first from pi_hot_first_perm; must be a permutation of
+ *         0..ffn-1.  The layer deals this order round-robin over G slices,
+ *         G = the device's SM count: the k-th neuron of `perm` is stored in
+ *         slice k % G at place k / G, slices (sizes differing by at most one)
+ *         laid out one after another.  Every slice then holds the same mix of
+ *         hot and cold neurons, which balances the persistent step's per-SM
+ *         work.  pi_layer_perm returns the resulting storage order.
  * The library copies W_p1 as is, permutes the rows of W_up, W_gate, b, W_p2,
  * c_p, and stores W_down transposed and permuted as W_down^T [ffn, d] so that
  * each neuron's down weights are one contiguous row.  Peak device memory is
@@ -102,7 +108,7 @@ pi_status pi_layer_destroy(pi_layer *layer);
 pi_status pi_layer_info(const pi_layer *layer, int32_t *d, int32_t *ffn,
                         int32_t *rank, int32_t *act);
 
-/* Copy the layer's permutation (host int32 [ffn]): position k holds model
+/* Copy the layer's storage order (host int32 [ffn]): position k holds model
  * neuron perm[k].  Active-set indices returned by this library are positions
  * k, i.e. in permuted space. */
 pi_status pi_layer_perm(const pi_layer *layer, int32_t *perm);

@@ -50,3 +50,21 @@ def oracle_y_for_valid_set(L: O.OracleLayer, x, S_gpu):
     the oracle's own set at most on neurons inside the rounding band, where
     either decision is a correct result."""
     return O.sparse_ffn(L, x, np.asarray(S_gpu, dtype=np.int64))
+
+
+def dealt_order(order, G: int) -> np.ndarray:
+    """The layout a layer stores for a caller's neuron order: the k-th neuron
+    of `order` goes to SM slice k % G at place k // G (slices of near-equal
+    size, laid out one after another)."""
+    order = np.asarray(order)
+    ffn = order.shape[0]
+    q, rr = divmod(ffn, G)
+    out = np.empty_like(order)
+    for k in range(ffn):
+        c, j = k % G, k // G
+        out[c * q + min(c, rr) + j] = order[k]
+    return out
+
+
+def sm_count() -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count

@@ -7,7 +7,8 @@ import pytest
 import torch
 
 from oracle import ffn as O
-from tests.gpu_helpers import check_union_set, check_y, oracle_y_for_valid_set, to_dev
+from tests.gpu_helpers import (check_union_set, check_y, dealt_order, oracle_y_for_valid_set,
+                               sm_count, to_dev)
 from workload import LayerSpec, make_layer, make_tokens
 from workload.gen import make_exact_layer, make_exact_tokens
 
@@ -185,7 +186,11 @@ def test_permuted_layer(pi):
     t, L = _layer(LayerSpec(d=d, ffn=ffn, rank=r, mean_f=0.1), seed=37)
     perm = np.random.default_rng(4).permutation(ffn).astype(np.int32)
     layer = pi.Layer.from_dict(to_dev(t), perm=perm)
-    np.testing.assert_array_equal(layer.perm(), perm)
+    stored = layer.perm()
+    np.testing.assert_array_equal(stored, dealt_order(perm, sm_count()))
+    identity = pi.Layer.from_dict(to_dev(t)).perm()
+    np.testing.assert_array_equal(identity, dealt_order(np.arange(ffn), sm_count()))
+    perm = stored
     P = O.permute_layer(L, perm)
     X = make_tokens(d, 4, seed=41)
     for b in range(4):
