@@ -70,7 +70,7 @@ struct LayerDev {
 struct StackParams {
   int n_layers, d, ffn, rank;
   int G, staged, lanes_l, pf_rows, pf_next;
-  int off_flag, off_list, off_p1, off_p2;   // dynamic shared memory offsets
+  int off_flag, off_list, off_lb, off_x, off_c, off_b, off_p1, off_p2;   // shared memory offsets
   const __half *x;       // [n_layers, B, d]
   float *y;              // [n_layers, B, d]
   int32_t *count;        // [n_layers] or nullptr

@@ -109,19 +109,33 @@ __device__ unsigned long long g_phase_ts[3][16][16];
 #define PHASE_STAMP(l, ph) do {} while (0)
 #endif
 
-// Issue the predictor weights of layer Ld for this CTA into shared memory
-// (one thread): its W_p1 rows k = cta, cta+G, ... and its W_p2 slice.
-__device__ __forceinline__ void stage_predictor(const pi::LayerDev &Ld, int cta, int G, int d, int r,
-                                                int s0, int s1, __half *p1_s, __half *p2_s,
-                                                uint32_t mbar) {
-  int na = 0;
-  for (int k = cta; k < r; k += G) ++na;
+// Stage the inputs of one layer for this CTA into shared memory (one thread,
+// TMA bulk copies completing on `mbar`): the token rows x [NB, d], the CTA's
+// slices of c_p and b (from the 16-byte boundary at or below s0; the layer
+// allocation pads both vectors to 256 bytes, so the rounded-up end stays
+// inside it) and, when `with_pred`, its W_p1 rows k = cta, cta+G, ... and
+// its W_p2 slice.
+__device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half *x, int nb, int cta,
+                                            int G, int d, int r, int s0, int s1, bool with_pred,
+                                            __half *x_s, float *c_s, float *b_s, __half *p1_s,
+                                            __half *p2_s, uint32_t mbar) {
+  const int s0a = s0 & ~3;
+  const uint32_t cb_bytes = (uint32_t)(((s1 - s0a) + 3) & ~3) * 4u;
+  const uint32_t x_bytes = (uint32_t)nb * (uint32_t)d * 2u;
   const uint32_t row_bytes = (uint32_t)d * 2u;
-  const uint32_t p2_bytes = (uint32_t)(s1 - s0) * (uint32_t)r * 2u;
-  const uint32_t total = (uint32_t)na * row_bytes + p2_bytes;
+  const uint32_t p2_bytes = with_pred ? (uint32_t)(s1 - s0) * (uint32_t)r * 2u : 0u;
+  int na = 0;
+  if (with_pred)
+    for (int k = cta; k < r; k += G) ++na;
+  const uint32_t total = x_bytes + (cb_bytes ? 2u * cb_bytes : 0u) + (uint32_t)na * row_bytes + p2_bytes;
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(total) : "memory");
+  tma_load_1d(x_s, x, x_bytes, mbar);
+  if (cb_bytes) {
+    tma_load_1d(c_s, Ld.c_p + s0a, cb_bytes, mbar);
+    tma_load_1d(b_s, Ld.b + s0a, cb_bytes, mbar);
+  }
   int q = 0;
-  for (int k = cta; k < r; k += G, ++q)
+  for (int k = cta; q < na; k += G, ++q)
     tma_load_1d(p1_s + (size_t)q * d, Ld.W_p1 + (size_t)k * d, row_bytes, mbar);
   if (p2_bytes) tma_load_1d(p2_s, Ld.W_p2 + (size_t)s0 * r, p2_bytes, mbar);
 }
@@ -158,38 +172,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   float *h_s = reinterpret_cast<float *>(smem);                                     // [NB, r]
   unsigned char *flag_s = reinterpret_cast<unsigned char *>(smem) + p.off_flag;    // [slice]
   int *list_s = reinterpret_cast<int *>(smem + p.off_list);                        // [slice]
+  float *lb_s = reinterpret_cast<float *>(smem + p.off_lb);                        // [slice] b of list
+  __half *x_s = reinterpret_cast<__half *>(smem + p.off_x);                        // [NB, d]
+  float *c_s = reinterpret_cast<float *>(smem + p.off_c);                          // c_p slice
+  float *b_s = reinterpret_cast<float *>(smem + p.off_b);                          // b slice
   __half *p1_s = reinterpret_cast<__half *>(smem + p.off_p1);                      // [na_max, d]
   __half *p2_s = reinterpret_cast<__half *>(smem + p.off_p2);                      // [slice, r]
+  const int s0a = s0 & ~3;                       // c_s / b_s start at this neuron
 
-  if (p.staged) {
-    if (tid == 0) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar));
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    if (tid == 0) stage_predictor(p.layers[0], cta, G, d, r, s0, s1, p1_s, p2_s, mbar);
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  __syncthreads();
+  if (tid == 0)
+    stage_layer(p.layers[0], p.x, NB, cta, G, d, r, s0, s1, p.staged != 0, x_s, c_s, b_s, p1_s, p2_s, mbar);
 
   for (int l = 0; l < p.n_layers; ++l) {
     const pi::LayerDev &Ld = p.layers[l];
-    const __half *x = p.x + (size_t)l * NB * d;
     PHASE_STAMP(l, 0);
 
+    if (!mbar_wait(mbar, (uint32_t)(l & 1))) {
+      if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
+      mbar_wait(mbar, (uint32_t)(l & 1));     // let a copy still in flight land
+      return;
+    }
     uint4 xr[NB][CPT];
 #pragma unroll
     for (int t = 0; t < NB; ++t)
 #pragma unroll
       for (int c = 0; c < CPT; ++c) {
         const int v = tid + c * kThreads;
-        xr[t][c] = v < nv ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * d) + v)
+        xr[t][c] = v < nv ? reinterpret_cast<const uint4 *>(x_s + (size_t)t * d)[v]
                           : make_uint4(0, 0, 0, 0);
       }
-
-    if (p.staged && !mbar_wait(mbar, (uint32_t)(l & 1))) {
-      if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
-      mbar_wait(mbar, (uint32_t)(l & 1));     // let a copy still in flight land
-      return;
-    }
 
     // ---------------- A: h = ReLU(W_p1 x), rows cta, cta + G, ... (8 rows per pass)
     for (int q0 = 0; cta + q0 * G < r; q0 += 8) {
@@ -292,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           for (int t = 0; t < NB; ++t) {
             float s = acc[u][t];
             for (int o = GL >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (valid) on |= (s + Ld.c_p[s0 + rl]) > 0.f;
+            if (valid) on |= (s + c_s[s0 + rl - s0a]) > 0.f;
           }
           if (valid && sub == 0) flag_s[rl] = on ? 1 : 0;
         }
@@ -317,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         lcount += tot;
         __syncthreads();
       }
+      for (int j = tid; j < lcount; j += kThreads) lb_s[j] = b_s[list_s[j] - s0a];
       if (p.mask_out)
         for (int i = tid; i < n_rows; i += kThreads) p.mask_out[(size_t)l * ffn + s0 + i] = flag_s[i];
       if (tid == 0) p.cnt[cta] = lcount;
@@ -331,12 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     }
     PHASE_STAMP(l, 3);
 
-    // next layer's predictor weights: TMA into shared memory, or L2 prefetch
+    // next layer's inputs: TMA into shared memory (+ L2 prefetch of its
+    // predictor weights when they are not staged).  Every thread is done with
+    // x_s, c_s, b_s, p1_s and p2_s of this layer past this barrier.
+    __syncthreads();
     if (l + 1 < p.n_layers && tid == 0) {
       const pi::LayerDev &Ln = p.layers[l + 1];
-      if (p.staged) {
-        stage_predictor(Ln, cta, G, d, r, s0, s1, p1_s, p2_s, mbar);
-      } else if (p.pf_next) {
+      stage_layer(Ln, p.x + (size_t)(l + 1) * NB * d, NB, cta, G, d, r, s0, s1, p.staged != 0, x_s,
+                  c_s, b_s, p1_s, p2_s, mbar);
+      if (!p.staged && p.pf_next) {
         for (int k = cta; k < r; k += G) pidev::prefetch_l2_bulk(Ln.W_p1 + (size_t)k * d, row_bytes);
         const uint32_t p2_bytes = (uint32_t)n_rows * (uint32_t)r * 2u;
         const char *base = reinterpret_cast<const char *>(Ln.W_p2 + (size_t)s0 * r);
@@ -397,17 +417,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         const int t = tid / GW, n = tid % GW;
         float a = 0.f;
         if (n < n_here) {
-          const int i = list_s[w0 + n];
+          const float bi = lb_s[w0 + n];
           float su = 0.f, sg = 0.f;
           for (int q = 0; q < kWarps; ++q) {   // fixed order over warps
             su += red_s[q][t][0][n];
             if (REGLU) sg += red_s[q][t][NR - 1][n];
           }
           if (REGLU) {
-            const float gz = sg + Ld.b[i];
+            const float gz = sg + bi;
             a = (gz > 0.f ? gz : 0.f) * su;
           } else {
-            const float z = su + Ld.b[i];
+            const float z = su + bi;
             a = z > 0.f ? z : 0.f;
           }
         }
@@ -445,8 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     // group summing splits g, g+64, ... in order; then a fixed shuffle tree
     // over the 32 lanes of each warp, and the two warps of a column in order.
     if (cta == 0 && p.count && wid == 0) {
+      int cv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) cv[q] = q * 32 + lane < G ? ldcg(p.cnt + q * 32 + lane) : 0;
       int s = 0;
-      for (int c = lane; c < G; c += 32) s += ldcg(p.cnt + c);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) s += cv[q];
+      for (int c = 256 + lane; c < G; c += 32) s += ldcg(p.cnt + c);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       if (lane == 0) p.count[l] = s;
@@ -543,7 +568,7 @@ constexpr size_t kSmemBudget = 200 * 1024;   // dynamic shared memory the step m
 size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
 
 struct SmemPlan {
-  size_t off_flag, off_list, off_p1, off_p2, base_end, staged_end;
+  size_t off_flag, off_list, off_lb, off_x, off_c, off_b, off_p1, off_p2, base_end, staged_end;
 };
 
 SmemPlan smem_plan(const pi_layer *L, int B) {
@@ -554,6 +579,10 @@ SmemPlan smem_plan(const pi_layer *L, int B) {
   size_t off = align128(sizeof(float) * (size_t)B * L->rank);
   s.off_flag = off;  off = align128(off + slice);
   s.off_list = off;  off = align128(off + sizeof(int) * slice);
+  s.off_lb = off;    off = align128(off + sizeof(float) * slice);
+  s.off_x = off;     off = align128(off + 2 * (size_t)B * L->d);
+  s.off_c = off;     off = align128(off + sizeof(float) * (slice + 8));
+  s.off_b = off;     off = align128(off + sizeof(float) * (slice + 8));
   s.base_end = off;
   s.off_p1 = off;    off = align128(off + na_max * L->d * 2);
   s.off_p2 = off;    off = align128(off + slice * L->rank * 2);
@@ -589,6 +618,10 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   p.staged = step_staged(L0, B) ? 1 : 0;
   p.off_flag = (int)sp.off_flag;
   p.off_list = (int)sp.off_list;
+  p.off_lb = (int)sp.off_lb;
+  p.off_x = (int)sp.off_x;
+  p.off_c = (int)sp.off_c;
+  p.off_b = (int)sp.off_b;
   p.off_p1 = (int)sp.off_p1;
   p.off_p2 = (int)sp.off_p2;
   int GL = 32;

@@ -8,6 +8,12 @@ ABS_TOL = 2e-3      # max abs error bound on y (fp16 weights, fp32 accumulation)
 REL_L2_TOL = 1e-3   # relative L2 error bound on y
 
 
+def stored_oracle(layer, t: dict) -> O.OracleLayer:
+    """The oracle for a GPU layer as it is stored: model-space weights put in
+    the layer's storage order (pi_layer_perm), so positions line up."""
+    return O.permute_layer(O.OracleLayer.from_tensors(t), layer.perm())
+
+
 def to_dev(t: dict, dev="cuda"):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
 

@@ -8,7 +8,7 @@ import torch
 
 from oracle import ffn as O
 from tests.gpu_helpers import (check_union_set, check_y, dealt_order, oracle_y_for_valid_set,
-                               sm_count, to_dev)
+                               sm_count, stored_oracle, to_dev)
 from workload import LayerSpec, make_layer, make_tokens
 from workload.gen import make_exact_layer, make_exact_tokens
 
@@ -43,9 +43,10 @@ SHAPES = [
 @pytest.mark.parametrize("B", [1, 3, 9])
 def test_predict(pi, shape, B):
     d, ffn, r, act = shape
-    t, L = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1), seed=d + B)
+    t, _ = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1), seed=d + B)
     x = make_tokens(d, B, seed=5 + B)
     layer = pi.Layer.from_dict(to_dev(t))
+    L = stored_oracle(layer, t)
     mask, logits = layer.predict(x.cuda(), want_logits=True)
     torch.cuda.synchronize()
     l_gpu = logits.cpu().numpy().astype(np.float64)
@@ -84,10 +85,11 @@ def test_compact(pi, ffn, B):
 @pytest.mark.parametrize("B", [1, 2, 3, 5])
 def test_sparse_ffn(pi, shape, B):
     d, ffn, r, act = shape
-    t, L = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.12), seed=7 * d + B)
+    t, _ = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.12), seed=7 * d + B)
     x = make_tokens(d, B, seed=11 + B)
-    S = O.predicted_forward(L, x)["S"]             # the oracle's own set as input
     layer = pi.Layer.from_dict(to_dev(t))
+    L = stored_oracle(layer, t)
+    S = O.predicted_forward(L, x)["S"]             # the oracle's own set as input
     idx = torch.from_numpy(S.astype(np.int32)).cuda()
     count = torch.tensor([S.size], dtype=torch.int32, device="cuda")
     y = layer.sparse_ffn(x.cuda(), idx, count)
@@ -102,9 +104,10 @@ def test_sparse_ffn(pi, shape, B):
 @pytest.mark.parametrize("B", [1, 4])
 def test_dense_ref_and_exact_mask(pi, shape, B):
     d, ffn, r, act = shape
-    t, L = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1), seed=13 * d + B)
+    t, _ = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1), seed=13 * d + B)
     x = make_tokens(d, B, seed=17 + B)
     layer = pi.Layer.from_dict(to_dev(t))
+    L = stored_oracle(layer, t)
     yd = layer.dense_ref(x.cuda())
     m, _ = O.exact_mask(L, x)
     S = O.active_union(m)
@@ -126,7 +129,7 @@ def test_rows_outside_set_are_never_read(pi, act):
     torch.cuda.synchronize()
     S = idx[:int(count.item())].cpu().numpy()
     y0 = clean.sparse_ffn(x, torch.from_numpy(S.astype(np.int32)).cuda(), count)
-    out = torch.from_numpy(np.setdiff1d(np.arange(ffn), S))
+    out = torch.from_numpy(clean.perm()[np.setdiff1d(np.arange(ffn), S)].astype(np.int64))
     p = dict(t)
     p["W_up"] = t["W_up"].clone(); p["W_up"][out] = float("nan")
     p["W_down"] = t["W_down"].clone(); p["W_down"][:, out] = float("inf")
@@ -146,9 +149,9 @@ def test_exact_arithmetic_bitwise(pi, act, B):
     """Integer-grid data: every binary32 sum is exact, so the GPU must match the
     oracle bit for bit (set and output) whatever its summation order."""
     t = make_exact_layer(1024, 2048, 64, act=act, seed=5)
-    L = O.OracleLayer.from_tensors(t)
     X = make_exact_tokens(1024, B, seed=6)
     layer = pi.Layer.from_dict(to_dev(t))
+    L = stored_oracle(layer, t)
     y, idx, count = layer.forward(X.cuda())
     torch.cuda.synchronize()
     r = O.predicted_forward(L, X)
@@ -161,8 +164,9 @@ def test_exact_arithmetic_bitwise(pi, act, B):
 
 def test_empty_set_and_bad_inputs(pi):
     d, ffn, r = 1024, 4096, 64
-    t, L = _layer(LayerSpec(d=d, ffn=ffn, rank=r), seed=29)
+    t, _ = _layer(LayerSpec(d=d, ffn=ffn, rank=r), seed=29)
     layer = pi.Layer.from_dict(to_dev(t))
+    L = stored_oracle(layer, t)
     x = make_tokens(d, 1, seed=31)
     xc = x.cuda()
     idx = torch.arange(ffn, dtype=torch.int32, device="cuda")
@@ -209,8 +213,9 @@ def test_permuted_layer(pi):
 @pytest.mark.parametrize("B", [1, 2, 4])
 def test_layer_forward_single_opt_layer(pi, B):
     """The single OPT-style layer workload: d=1024, ffn=4096, r=64, 64 tokens."""
-    t, L = _layer(LayerSpec(d=1024, ffn=4096, rank=64, mean_f=0.10), seed=1001)
+    t, _ = _layer(LayerSpec(d=1024, ffn=4096, rank=64, mean_f=0.10), seed=1001)
     layer = pi.Layer.from_dict(to_dev(t))
+    L = stored_oracle(layer, t)
     X = make_tokens(1024, 64, seed=1001)
     band = 0
     for s in range(0, 64, B):

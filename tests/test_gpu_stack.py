@@ -55,7 +55,7 @@ def test_stack_forward(pi, act, d, ffn, r, B):
     for l in range(n):
         c = int(count[l].item())
         S = idx[l, :c].cpu().numpy().astype(np.int64)
-        _check_layer(ts[l], x[l], y[l].cpu().numpy(), S)
+        _check_layer(ts[l], x[l], y[l].cpu().numpy(), S, perm=layers[l].perm())
     assert layers[0].device_status() == 0
 
 
@@ -72,7 +72,8 @@ def test_long_stack_spans_launches(pi):
     torch.cuda.synchronize()
     for l in range(n):
         c = int(count[l].item())
-        _check_layer(ts[l], x[l], y[l].cpu().numpy(), idx[l, :c].cpu().numpy().astype(np.int64))
+        _check_layer(ts[l], x[l], y[l].cpu().numpy(), idx[l, :c].cpu().numpy().astype(np.int64),
+                     perm=layers[l].perm())
     assert layers[0].device_status() == 0
 
 
@@ -140,7 +141,7 @@ def test_full_size_layer(pi, name):
     layer = pi.Layer.from_dict(t)
     th = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
     del t
-    L = O.OracleLayer.from_tensors(th)
+    L = O.permute_layer(O.OracleLayer.from_tensors(th), layer.perm())
     for B in sorted(set((1,) + tuple(b for b in cfg.batches if b > 1))):
         x = make_tokens(spec.d, B, seed=sub_seed(cfg.seed, B, "full_size_x"))
         y, idx, count = layer.forward(x.to(dev))
