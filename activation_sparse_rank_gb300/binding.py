@@ -50,6 +50,7 @@ _SIG = {
     "pi_predict": (C.c_int, [_p, _p, _i32, _p, _p, _p, C.c_size_t, _p]),
     "pi_compact_active": (C.c_int, [_p, _p, _i32, _p, _p, _p]),
     "pi_sparse_ffn": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
+    "pi_sparse_ffn_noalloc": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p]),
     "pi_ffn_dense_ref": (C.c_int, [_p, _p, _i32, _p, _p, C.c_size_t, _p]),
     "pi_layer_forward": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
     "pi_stack_forward": (C.c_int, [_p, _i32, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),

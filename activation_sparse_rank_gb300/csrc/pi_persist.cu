@@ -105,8 +105,22 @@ __device__ unsigned long long g_phase_ts[3][16][16];
       g_phase_ts[w_][l][ph] = t_;                                                 \
     }                                                                             \
   } while (0)
+// per CTA and layer: up/down phase duration (ns) and local active count
+__device__ unsigned long long g_cta_e[160][16][2];
+#define CTA_E_BEGIN(l) unsigned long long te0_ = 0; if (threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(te0_));
+#define CTA_E_END(l, cnt)                                                            \
+  do {                                                                               \
+    if (threadIdx.x == 0 && blockIdx.x < 160 && (l) < 16) {                          \
+      unsigned long long t_;                                                         \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                         \
+      g_cta_e[blockIdx.x][l][0] = t_ - te0_;                                         \
+      g_cta_e[blockIdx.x][l][1] = (unsigned long long)(cnt);                         \
+    }                                                                                \
+  } while (0)
 #else
 #define PHASE_STAMP(l, ph) do {} while (0)
+#define CTA_E_BEGIN(l) do {} while (0)
+#define CTA_E_END(l, cnt) do {} while (0)
 #endif
 
 // Stage the inputs of one layer for this CTA into shared memory (one thread,
@@ -257,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     // ---------------- C: logits over my slice, ordered local active list
     for (int e = tid; e < NB * r; e += kThreads) h_s[e] = ldcg(p.h + e);
     __syncthreads();
+    PHASE_STAMP(l, 9);
     {
       const int GL = p.lanes_l;                 // lanes per predictor row (8, 16, 32)
       const int rows_per_warp = 32 / GL;
@@ -315,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       }
     }
     __syncthreads();
+    PHASE_STAMP(l, 10);
     int lcount = 0;
     {
       for (int c0 = 0; c0 < n_rows; c0 += kThreads) {
@@ -333,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         lcount += tot;
         __syncthreads();
       }
+      PHASE_STAMP(l, 11);
       for (int j = tid; j < lcount; j += kThreads) lb_s[j] = b_s[list_s[j] - s0a];
       if (p.mask_out)
         for (int i = tid; i < n_rows; i += kThreads) p.mask_out[(size_t)l * ffn + s0 + i] = flag_s[i];
@@ -347,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       }
     }
     PHASE_STAMP(l, 3);
+    CTA_E_BEGIN(l);
 
     // next layer's inputs: TMA into shared memory (+ L2 prefetch of its
     // predictor weights when they are not staged).  Every thread is done with
@@ -445,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       __syncthreads();   // red_s / a_s are rewritten by the next window
     }
     PHASE_STAMP(l, 4);
+    CTA_E_END(l, lcount);
 #pragma unroll
     for (int t = 0; t < NB; ++t)
 #pragma unroll
@@ -525,6 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
 }  // namespace
 extern "C" int pi_debug_phase_times(unsigned long long *out) {
   return (int)cudaMemcpyFromSymbol(out, g_phase_ts, sizeof(g_phase_ts));
+}
+extern "C" int pi_debug_cta_e(unsigned long long *out) {
+  return (int)cudaMemcpyFromSymbol(out, g_cta_e, sizeof(g_cta_e));
 }
 namespace {
 #endif

@@ -194,6 +194,27 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers,
                            int32_t *count, float *y, void *ws,
                            size_t ws_bytes, void *stream);
 
+/* pi_sparse_ffn without a workspace, for callers that cannot allocate device
+ * memory when they call in (for example a serving framework that has already
+ * handed all GPU memory to its own pool, or a plug-in that receives only input
+ * and output pointers).  The pages have no counterpart: this is a calling
+ * convention of this library, not part of the method.
+ * Same arguments and results as pi_sparse_ffn (x, idx, count, y device
+ * pointers), batches of 1 or 2 tokens only.  The split partial sums live in a
+ * fixed 16 MiB device array inside the library (reserved on every GPU that
+ * loads it, until the process exits); a call whose d and B need more than
+ * that (4 * splits * B * d bytes, splits = the SM count, or 4x it for d < 4096)
+ * returns PI_ERR_UNSUPPORTED without launching.  Nothing is allocated and
+ * nothing in the array has to start at zero.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call outside any
+ * stream capture.  All calls share the one array: calls whose kernels can
+ * overlap on the GPU (other streams, other host threads) race on it and must
+ * be serialised by the caller. */
+pi_status pi_sparse_ffn_noalloc(pi_layer *layer, const uint16_t *x, int32_t B,
+                                const int32_t *idx, const int32_t *count, float *y,
+                                void *stream);
+
 /* Offline activation profile (section 2.3, core module 1 "LLM profiler";
  * section 2.2, profiling data): for T tokens x_t, in model space,
  *   counts[i] += #{t : z_i(x_t) > 0}, z = W_up x + b (ReLU) or W_gate x + b (ReGLU)
