@@ -70,7 +70,8 @@ struct LayerDev {
 struct StackParams {
   int n_layers, d, ffn, rank;
   int G, staged, lanes_l, pf_rows, pf_next;
-  int off_flag, off_list, off_lb, off_x, off_c, off_b, off_p1, off_p2;   // shared memory offsets
+  int off_flag, off_list, off_lb, off_stage, stage_bytes;   // shared memory layout
+  int soff_c, soff_b, soff_p1, soff_p2;                     // offsets inside a stage buffer
   const __half *x;       // [n_layers, B, d]
   float *y;              // [n_layers, B, d]
   int32_t *count;        // [n_layers] or nullptr

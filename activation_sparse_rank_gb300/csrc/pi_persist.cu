@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   __shared__ float ared_s[kWarps][NB][8];
   __shared__ float4 fred_s[2][8];
   __shared__ int wtot_s[kWarps];
-  __shared__ __align__(8) unsigned long long mbar_s;
+  __shared__ __align__(8) unsigned long long mbar_s[2];
 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   const uint32_t row_bytes = (uint32_t)d * 2u;
   unsigned *status = p.status;
   unsigned epoch = 0;
-  const uint32_t mbar = smem_u32(&mbar_s);
+  const uint32_t mbar0 = smem_u32(&mbar_s[0]);
 
   // this CTA's neuron slice [s0, s1): sizes differ by at most one
   const int q_sl = ffn / G, r_sl = ffn % G;
@@ -187,30 +187,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   unsigned char *flag_s = reinterpret_cast<unsigned char *>(smem) + p.off_flag;    // [slice]
   int *list_s = reinterpret_cast<int *>(smem + p.off_list);                        // [slice]
   float *lb_s = reinterpret_cast<float *>(smem + p.off_lb);                        // [slice] b of list
-  __half *x_s = reinterpret_cast<__half *>(smem + p.off_x);                        // [NB, d]
-  float *c_s = reinterpret_cast<float *>(smem + p.off_c);                          // c_p slice
-  float *b_s = reinterpret_cast<float *>(smem + p.off_b);                          // b slice
-  __half *p1_s = reinterpret_cast<__half *>(smem + p.off_p1);                      // [na_max, d]
-  __half *p2_s = reinterpret_cast<__half *>(smem + p.off_p2);                      // [slice, r]
-  const int s0a = s0 & ~3;                       // c_s / b_s start at this neuron
+  // two stage buffers (layer l uses buffer l & 1), each [x | c_p slice | b slice | W_p1 rows | W_p2 slice]
+  auto stage_buf = [&](int k) { return smem + p.off_stage + (size_t)k * p.stage_bytes; };
+  const int s0a = s0 & ~3;                       // c / b slices start at this neuron
+  auto stage = [&](int layer) {                  // one thread: issue layer's inputs into its buffer
+    unsigned char *bsm = stage_buf(layer & 1);
+    stage_layer(p.layers[layer], p.x + (size_t)layer * NB * d, NB, cta, G, d, r, s0, s1,
+                p.staged != 0, reinterpret_cast<__half *>(bsm), reinterpret_cast<float *>(bsm + p.soff_c),
+                reinterpret_cast<float *>(bsm + p.soff_b), reinterpret_cast<__half *>(bsm + p.soff_p1),
+                reinterpret_cast<__half *>(bsm + p.soff_p2), mbar0 + 8u * (uint32_t)(layer & 1));
+  };
 
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8u));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (tid == 0)
-    stage_layer(p.layers[0], p.x, NB, cta, G, d, r, s0, s1, p.staged != 0, x_s, c_s, b_s, p1_s, p2_s, mbar);
+  if (tid == 0) stage(0);
 
   for (int l = 0; l < p.n_layers; ++l) {
     const pi::LayerDev &Ld = p.layers[l];
     PHASE_STAMP(l, 0);
 
-    if (!mbar_wait(mbar, (uint32_t)(l & 1))) {
+    const uint32_t mbar = mbar0 + 8u * (uint32_t)(l & 1);
+    // the next layer's inputs go to the other buffer, free since the last barrier
+    if (tid == 0 && l + 1 < p.n_layers) stage(l + 1);
+    if (!mbar_wait(mbar, (uint32_t)((l >> 1) & 1))) {
       if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
-      mbar_wait(mbar, (uint32_t)(l & 1));     // let a copy still in flight land
+      mbar_wait(mbar, (uint32_t)((l >> 1) & 1));            // let a copy in flight land
+      if (l + 1 < p.n_layers) mbar_wait(mbar0 + 8u * (uint32_t)((l + 1) & 1), (uint32_t)(((l + 1) >> 1) & 1));
       return;
     }
+    unsigned char *bsm = stage_buf(l & 1);
+    const __half *x_s = reinterpret_cast<const __half *>(bsm);
+    const float *c_s = reinterpret_cast<const float *>(bsm + p.soff_c);
+    const float *b_s = reinterpret_cast<const float *>(bsm + p.soff_b);
+    const __half *p1_s = reinterpret_cast<const __half *>(bsm + p.soff_p1);
+    const __half *p2_s = reinterpret_cast<const __half *>(bsm + p.soff_p2);
     uint4 xr[NB][CPT];
 #pragma unroll
     for (int t = 0; t < NB; ++t)
@@ -314,18 +328,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
             }
           }
         }
+        // reduce-scatter of the 8 rows' partial sums over the GL lanes of the
+        // row group: 3 halving exchanges leave each lane one row (bits o1, o2,
+        // o3 of the lane pick it), then a plain reduction over the low bits.
+        const int o1 = GL >> 1, o2 = GL >> 2, o3 = GL >> 3;
+        const bool b1 = (lane & o1) != 0, b2 = (lane & o2) != 0, b3 = (lane & o3) != 0;
+        bool on = false;
 #pragma unroll
-        for (int u = 0; u < RU; ++u) {
-          const int rl = ((it0 + u) * kWarps + wid) * rows_per_warp + lane / GL;
-          const bool valid = it0 + u < iters && rl < n_rows;
-          bool on = false;
+        for (int t = 0; t < NB; ++t) {
+          float k4[4], k2[2];
 #pragma unroll
-          for (int t = 0; t < NB; ++t) {
-            float s = acc[u][t];
-            for (int o = GL >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (valid) on |= (s + c_s[s0 + rl - s0a]) > 0.f;
+          for (int j = 0; j < 4; ++j) {
+            const float mine = b1 ? acc[j + 4][t] : acc[j][t];
+            const float oth = b1 ? acc[j][t] : acc[j + 4][t];
+            k4[j] = mine + __shfl_xor_sync(0xffffffffu, oth, o1);
           }
-          if (valid && sub == 0) flag_s[rl] = on ? 1 : 0;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float mine = b2 ? k4[j + 2] : k4[j];
+            const float oth = b2 ? k4[j] : k4[j + 2];
+            k2[j] = mine + __shfl_xor_sync(0xffffffffu, oth, o2);
+          }
+          float k1 = (b3 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, b3 ? k2[0] : k2[1], o3);
+          for (int o = o3 >> 1; o > 0; o >>= 1) k1 += __shfl_xor_sync(0xffffffffu, k1, o);
+          const int u = (b1 ? 4 : 0) + (b2 ? 2 : 0) + (b3 ? 1 : 0);
+          const int rl = ((it0 + u) * kWarps + wid) * rows_per_warp + lane / GL;
+          if (it0 + u < iters && rl < n_rows) on |= (k1 + c_s[s0 + rl - s0a]) > 0.f;
+        }
+        {
+          const int u = (b1 ? 4 : 0) + (b2 ? 2 : 0) + (b3 ? 1 : 0);
+          const int rl = ((it0 + u) * kWarps + wid) * rows_per_warp + lane / GL;
+          if ((lane & (o3 - 1)) == 0 && it0 + u < iters && rl < n_rows) flag_s[rl] = on ? 1 : 0;
         }
       }
     }
@@ -350,10 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         __syncthreads();
       }
       PHASE_STAMP(l, 11);
-      for (int j = tid; j < lcount; j += kThreads) lb_s[j] = b_s[list_s[j] - s0a];
-      if (p.mask_out)
-        for (int i = tid; i < n_rows; i += kThreads) p.mask_out[(size_t)l * ffn + s0 + i] = flag_s[i];
-      if (tid == 0) p.cnt[cta] = lcount;
       // ask L2 for all my active rows now (bounded by the prefetch budget)
       const int npf = min(lcount, p.pf_rows);
       for (int j = tid; j < npf; j += kThreads) {
@@ -362,26 +391,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
         pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
       }
+      for (int j = tid; j < lcount; j += kThreads) lb_s[j] = b_s[list_s[j] - s0a];
+      if (p.mask_out)
+        for (int i = tid; i < n_rows; i += kThreads) p.mask_out[(size_t)l * ffn + s0 + i] = flag_s[i];
+      if (tid == 0) p.cnt[cta] = lcount;
     }
+    // unstaged predictor weights of the next layer: ask L2 for them now
+    if (!p.staged && p.pf_next && l + 1 < p.n_layers && tid == 0) {
+      const pi::LayerDev &Ln = p.layers[l + 1];
+      for (int k = cta; k < r; k += G) pidev::prefetch_l2_bulk(Ln.W_p1 + (size_t)k * d, row_bytes);
+      const uint32_t p2_bytes = (uint32_t)n_rows * (uint32_t)r * 2u;
+      const char *base = reinterpret_cast<const char *>(Ln.W_p2 + (size_t)s0 * r);
+      for (uint32_t o = 0; o < p2_bytes; o += 65536u)
+        pidev::prefetch_l2_bulk(base + o, min(65536u, p2_bytes - o));
+    }
+    __syncthreads();
     PHASE_STAMP(l, 3);
     CTA_E_BEGIN(l);
-
-    // next layer's inputs: TMA into shared memory (+ L2 prefetch of its
-    // predictor weights when they are not staged).  Every thread is done with
-    // x_s, c_s, b_s, p1_s and p2_s of this layer past this barrier.
-    __syncthreads();
-    if (l + 1 < p.n_layers && tid == 0) {
-      const pi::LayerDev &Ln = p.layers[l + 1];
-      stage_layer(Ln, p.x + (size_t)(l + 1) * NB * d, NB, cta, G, d, r, s0, s1, p.staged != 0, x_s,
-                  c_s, b_s, p1_s, p2_s, mbar);
-      if (!p.staged && p.pf_next) {
-        for (int k = cta; k < r; k += G) pidev::prefetch_l2_bulk(Ln.W_p1 + (size_t)k * d, row_bytes);
-        const uint32_t p2_bytes = (uint32_t)n_rows * (uint32_t)r * 2u;
-        const char *base = reinterpret_cast<const char *>(Ln.W_p2 + (size_t)s0 * r);
-        for (uint32_t o = 0; o < p2_bytes; o += 65536u)
-          pidev::prefetch_l2_bulk(base + o, min(65536u, p2_bytes - o));
-      }
-    }
 
     // ---------------- E: up (+gate) and down rows of my active neurons
     float acc[NB][CPT][8];
@@ -590,7 +616,10 @@ constexpr size_t kSmemBudget = 200 * 1024;   // dynamic shared memory the step m
 size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
 
 struct SmemPlan {
-  size_t off_flag, off_list, off_lb, off_x, off_c, off_b, off_p1, off_p2, base_end, staged_end;
+  size_t off_flag, off_list, off_lb, off_stage;          // absolute offsets
+  size_t soff_c, soff_b, soff_p1, soff_p2;              // offsets inside a stage buffer
+  size_t stage_small, stage_full;                        // buffer size without / with predictor
+  size_t base_end;
 };
 
 SmemPlan smem_plan(const pi_layer *L, int B) {
@@ -598,17 +627,19 @@ SmemPlan smem_plan(const pi_layer *L, int B) {
   const size_t slice = (size_t)pi::step_slice(L);
   const size_t na_max = (size_t)(L->rank + G - 1) / G;
   SmemPlan s;
-  size_t off = align128(sizeof(float) * (size_t)B * L->rank);
+  size_t off = align128(sizeof(float) * (size_t)B * L->rank);   // h
   s.off_flag = off;  off = align128(off + slice);
   s.off_list = off;  off = align128(off + sizeof(int) * slice);
   s.off_lb = off;    off = align128(off + sizeof(float) * slice);
-  s.off_x = off;     off = align128(off + 2 * (size_t)B * L->d);
-  s.off_c = off;     off = align128(off + sizeof(float) * (slice + 8));
-  s.off_b = off;     off = align128(off + sizeof(float) * (slice + 8));
+  s.off_stage = off;
   s.base_end = off;
-  s.off_p1 = off;    off = align128(off + na_max * L->d * 2);
-  s.off_p2 = off;    off = align128(off + slice * L->rank * 2);
-  s.staged_end = off;
+  size_t so = align128(2 * (size_t)B * L->d);                     // x
+  s.soff_c = so;     so = align128(so + sizeof(float) * (slice + 8));
+  s.soff_b = so;     so = align128(so + sizeof(float) * (slice + 8));
+  s.stage_small = so;
+  s.soff_p1 = so;    so = align128(so + na_max * L->d * 2);
+  s.soff_p2 = so;    so = align128(so + slice * L->rank * 2);
+  s.stage_full = so;
   return s;
 }
 
@@ -620,11 +651,14 @@ int step_grid(const pi_layer *L) { return L->num_sms; }
 
 int step_slice(const pi_layer *L) { return (L->ffn + step_grid(L) - 1) / step_grid(L); }
 
-bool step_staged(const pi_layer *L, int B) { return smem_plan(L, B).staged_end <= kSmemBudget; }
+bool step_staged(const pi_layer *L, int B) {
+  const SmemPlan s = smem_plan(L, B);
+  return s.base_end + 2 * s.stage_full <= kSmemBudget;
+}
 
 size_t step_smem(const pi_layer *L, int B) {
   const SmemPlan s = smem_plan(L, B);
-  return s.staged_end <= kSmemBudget ? s.staged_end : s.base_end;
+  return s.base_end + 2 * (step_staged(L, B) ? s.stage_full : s.stage_small);
 }
 
 cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, int32_t *idx,
@@ -641,11 +675,12 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   p.off_flag = (int)sp.off_flag;
   p.off_list = (int)sp.off_list;
   p.off_lb = (int)sp.off_lb;
-  p.off_x = (int)sp.off_x;
-  p.off_c = (int)sp.off_c;
-  p.off_b = (int)sp.off_b;
-  p.off_p1 = (int)sp.off_p1;
-  p.off_p2 = (int)sp.off_p2;
+  p.off_stage = (int)sp.off_stage;
+  p.stage_bytes = (int)(p.staged ? sp.stage_full : sp.stage_small);
+  p.soff_c = (int)sp.soff_c;
+  p.soff_b = (int)sp.soff_b;
+  p.soff_p1 = (int)sp.soff_p1;
+  p.soff_p2 = (int)sp.soff_p2;
   int GL = 32;
   while (GL > 8 && GL * 8 > L0->rank) GL >>= 1;
   p.lanes_l = GL;
