@@ -59,6 +59,7 @@ _SIG = {
     "pi_device_status": (C.c_int, [_p, _p]),
     "pi_layer_set_timing_events": (C.c_int, [_p, _p, _p]),
     "pi_forward_launches": (C.c_int32, [_p, _i32]),
+    "pi_layer_set_hot_count": (C.c_int, [_p, _i32]),
     "pi_last_error": (C.c_char_p, []),
     "pi_status_string": (C.c_char_p, [C.c_int]),
 }
@@ -242,6 +243,10 @@ class Layer:
         b = None if before is None else C.c_void_p(before.cuda_event)
         a = None if after is None else C.c_void_p(after.cuda_event)
         _check(lib.pi_layer_set_timing_events(self._h, b, a), "pi_layer_set_timing_events")
+
+    def set_hot_count(self, n_hot: int):
+        """Number of leading neurons of the creation order treated as hot."""
+        _check(lib.pi_layer_set_hot_count(self._h, int(n_hot)), "pi_layer_set_hot_count")
 
     def forward_launches(self, B: int) -> int:
         return int(lib.pi_forward_launches(self._h, int(B)))

@@ -537,6 +537,14 @@ pi_status pi_layer_set_timing_events(pi_layer *L, void *ev_before, void *ev_afte
   return PI_OK;
 }
 
+pi_status pi_layer_set_hot_count(pi_layer *L, int32_t n_hot) {
+  g_err[0] = 0;
+  if (!L) return pi::fail(PI_ERR_INVALID_ARG, "layer is NULL");
+  if (n_hot < 0 || n_hot > L->ffn) return pi::fail(PI_ERR_INVALID_ARG, "n_hot=%d outside [0, ffn]", n_hot);
+  L->n_hot = n_hot;
+  return PI_OK;
+}
+
 int32_t pi_forward_launches(const pi_layer *L, int32_t B) {
   if (!L || B < 1 || B > PI_MAX_BATCH) return 0;
   // B <= 2: one persistent cooperative launch (after a barrier-counter memset);

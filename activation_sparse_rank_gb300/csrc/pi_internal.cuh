@@ -29,6 +29,7 @@ struct pi_layer {
   unsigned int *status = nullptr;
   std::vector<int32_t> perm;     // host copy of the permutation
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;   // profiling hook
+  int n_hot = 0;                 // leading neurons of the caller's order treated as hot
 };
 
 namespace pi {
@@ -64,6 +65,7 @@ constexpr int kMaxStack = 64;
 struct LayerDev {
   const __half *W_p1, *W_p2, *W_up, *W_gate, *W_dT;
   const float *b, *c_p;
+  int hot_per_slice;     // leading slice positions whose rows are fetched speculatively
 };
 
 // Kernel parameters of the persistent step (passed by value, < 4 KB).

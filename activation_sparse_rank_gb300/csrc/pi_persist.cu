@@ -213,6 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     const uint32_t mbar = mbar0 + 8u * (uint32_t)(l & 1);
     // the next layer's inputs go to the other buffer, free since the last barrier
     if (tid == 0 && l + 1 < p.n_layers) stage(l + 1);
+    // Hot neurons (the leading places of the slice, from the offline profile)
+    // fire on most tokens: start their rows towards L2 now, while HBM would
+    // otherwise idle through the predictor phases.
+    const int n_hot = min(Ld.hot_per_slice, n_rows);
+    if (tid >= 32 && tid < 32 + n_hot) {
+      const int i = s0 + tid - 32;
+      pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
+      if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
+      pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+    }
     if (!mbar_wait(mbar, (uint32_t)((l >> 1) & 1))) {
       if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
       mbar_wait(mbar, (uint32_t)((l >> 1) & 1));            // let a copy in flight land
@@ -387,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       const int npf = min(lcount, p.pf_rows);
       for (int j = tid; j < npf; j += kThreads) {
         const int i = list_s[j];
+        if (i - s0 < n_hot) continue;          // requested at layer start
         pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
         if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
         pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
@@ -701,7 +712,10 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   p.status = L0->status;
   for (int l = 0; l < n; ++l) {
     const pi_layer *Ll = layers[l];
-    p.layers[l] = LayerDev{Ll->W_p1, Ll->W_p2, Ll->W_up, Ll->W_gate, Ll->W_dT, Ll->b, Ll->c_p};
+    // the k-th neuron of the caller's order sits at slice k % G, place k / G:
+    // the first n_hot of them fill places 0 .. ceil(n_hot / G) - 1 of the slices
+    const int hot = (Ll->n_hot + p.G - 1) / p.G;
+    p.layers[l] = LayerDev{Ll->W_p1, Ll->W_p2, Ll->W_up, Ll->W_gate, Ll->W_dT, Ll->b, Ll->c_p, hot};
   }
   cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return e;

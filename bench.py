@@ -134,12 +134,17 @@ def build_stack(cfg, device, n_layers, keep_host_layers):
     for l in range(n_layers):
         t = make_layer(spec, cfg.seed, l, device=device)
         perm = None
+        n_hot = 0
         if cfg.profile_tokens:
             Xp = make_tokens(spec.d, cfg.profile_tokens, sub_seed(cfg.seed, l, "profile"), device)
-            counts = pi.profile_activations(t, Xp)
-            perm = pi.hot_first_perm(counts.cpu().numpy())
+            counts = pi.profile_activations(t, Xp).cpu().numpy()
+            perm = pi.hot_first_perm(counts)
+            # hot: active on more than half of the profiled tokens
+            n_hot = int((counts > cfg.profile_tokens // 2).sum())
             del Xp
-        layers.append(pi.Layer.from_dict(t, perm=perm))
+        layer = pi.Layer.from_dict(t, perm=perm)
+        layer.set_hot_count(n_hot)
+        layers.append(layer)
         if l < keep_host_layers:
             host_layers.append({k: (v.cpu() if isinstance(v, torch.Tensor) else v)
                                 for k, v in t.items()})

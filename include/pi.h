@@ -240,6 +240,17 @@ pi_status pi_hot_first_perm(const int32_t *counts, int32_t ffn, int32_t *perm);
  * NULL switches it off.  The setting is per layer and read at call time. */
 pi_status pi_layer_set_timing_events(pi_layer *layer, void *ev_before, void *ev_after);
 
+/* Hot-neuron hint for the persistent step (section 2.3, variable table: hot
+ * neurons are the few that are activated most often; section 3.1 Finding 1).
+ * n_hot = how many leading neurons of the order given to pi_layer_create are
+ * hot (e.g. those a profile shows active on more than half of the tokens).
+ * pi_layer_forward / pi_stack_forward (B <= 2) then start streaming those
+ * neurons' rows towards L2 at the start of the layer, before the predictor
+ * has decided, so that HBM is busy during the predictor phases.  Results do
+ * not change; a hot neuron the predictor leaves out only costs bandwidth.
+ * 0 (the default) disables it.  0 <= n_hot <= ffn. */
+pi_status pi_layer_set_hot_count(pi_layer *layer, int32_t n_hot);
+
 /* Number of kernel launches one pi_layer_forward call makes for a batch of B
  * tokens (0 on bad arguments). */
 int32_t pi_forward_launches(const pi_layer *layer, int32_t B);

@@ -153,3 +153,23 @@ def test_full_size_layer(pi, name):
         y_ref = O.sparse_ffn(L, x[rows], S)
         check_y(y.cpu().numpy()[rows], y_ref)
     assert layer.device_status() == 0
+
+
+def test_hot_hint_changes_no_result(pi):
+    """The hot-neuron hint only moves data earlier: outputs are bitwise equal."""
+    spec = LayerSpec(d=2048, ffn=8192, rank=128, mean_f=0.1)
+    ts, layers = _stack(pi, spec, 3, seed=31)
+    x = make_tokens(2048, 3, seed=32).view(3, 1, 2048).cuda()
+    y0 = torch.empty(3, 1, 2048, dtype=torch.float32, device="cuda")
+    y1 = torch.empty_like(y0)
+    idx = torch.empty(3, 8192, dtype=torch.int32, device="cuda")
+    cnt0 = torch.empty(3, dtype=torch.int32, device="cuda")
+    cnt1 = torch.empty_like(cnt0)
+    pi.stack_forward(layers, x, y0, idx=idx, count=cnt0)
+    for l in layers:
+        l.set_hot_count(3000)
+    pi.stack_forward(layers, x, y1, idx=idx, count=cnt1)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(cnt0, cnt1)
+    with pytest.raises(pi.PiError):
+        layers[0].set_hot_count(8193)
