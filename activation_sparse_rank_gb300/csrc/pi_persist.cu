@@ -213,16 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     const uint32_t mbar = mbar0 + 8u * (uint32_t)(l & 1);
     // the next layer's inputs go to the other buffer, free since the last barrier
     if (tid == 0 && l + 1 < p.n_layers) stage(l + 1);
-    // Hot neurons (the leading places of the slice, from the offline profile)
-    // fire on most tokens: start their rows towards L2 now, while HBM would
-    // otherwise idle through the predictor phases.
     const int n_hot = min(Ld.hot_per_slice, n_rows);
-    if (tid >= 32 && tid < 32 + n_hot) {
-      const int i = s0 + tid - 32;
-      pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
-      if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
-      pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
-    }
     if (!mbar_wait(mbar, (uint32_t)((l >> 1) & 1))) {
       if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
       mbar_wait(mbar, (uint32_t)((l >> 1) & 1));            // let a copy in flight land
@@ -293,6 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     PHASE_STAMP(l, 2);
 
     // ---------------- C: logits over my slice, ordered local active list
+    // Hot neurons (the leading places of the slice, from the offline profile)
+    // fire on most tokens: start their rows towards L2 now, while HBM would
+    // otherwise idle through the logits.  (Issued after barrier 1: a burst
+    // before it slowed the barrier itself.)
+    if (tid >= 32 && tid < 32 + n_hot) {
+      const int i = s0 + tid - 32;
+      pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
+      if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
+      pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+    }
     for (int e = tid; e < NB * r; e += kThreads) h_s[e] = ldcg(p.h + e);
     __syncthreads();
     PHASE_STAMP(l, 9);

@@ -18,7 +18,7 @@ from .binding import Layer, stack_forward
 
 
 class SparseFFNStack:
-    def __init__(self, layers: List[Layer], tokens: int, B: int = 1):
+    def __init__(self, layers: List[Layer], tokens: int, B: int = 1, want_idx: bool = False):
         if not layers:
             raise ValueError("empty stack")
         self.layers = layers
@@ -30,7 +30,10 @@ class SparseFFNStack:
         dev = layers[0].device
         self.device = dev
         self.ws = layers[0].workspace(B)
-        self.idx = torch.empty(self.L, self.ffn, dtype=torch.int32, device=dev)
+        # ascending active lists of the last token, only when asked for (B <= 2
+        # computes the counts without them; B > 2 always needs them)
+        self.want_idx = want_idx or B > 2
+        self.idx = torch.empty(self.L, self.ffn, dtype=torch.int32, device=dev) if self.want_idx else None
         self.count = torch.zeros(self.T, self.L, dtype=torch.int32, device=dev)
         self.x = torch.empty(self.T, self.L, B, self.d, dtype=torch.float16, device=dev)
         self.y = torch.empty(self.T, self.L, B, self.d, dtype=torch.float32, device=dev)
@@ -40,9 +43,10 @@ class SparseFFNStack:
 
     def launches_per_step(self) -> int:
         """Kernels of this library launched per step (memsets not counted)."""
-        per_token = 1 if self.B <= 2 else sum(l.forward_launches(self.B) for l in self.layers)
-        n_launch = -(-self.L // 64) if self.B <= 2 else 1
-        return per_token * n_launch * self.T
+        if self.B <= 2:
+            n_launch = -(-self.L // 64)
+            return (2 if self.want_idx else 1) * n_launch * self.T
+        return sum(l.forward_launches(self.B) for l in self.layers) * self.T
 
     def _token(self, t: int, stream):
         stack_forward(self.layers, self.x[t], self.y[t], idx=self.idx, count=self.count[t],

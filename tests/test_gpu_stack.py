@@ -110,7 +110,7 @@ def test_bench_configuration_sampled(pi):
     check_layers = [0, 13, 31]
     layers, _ = bench.build_stack(cfg, dev, cfg.layers, keep_host_layers=0)
     T = 3
-    st = SparseFFNStack(layers, tokens=T, B=1)
+    st = SparseFFNStack(layers, tokens=T, B=1, want_idx=True)
     X = make_tokens(spec.d, T * cfg.layers, sub_seed(cfg.seed, 1000, "bench_x"), dev)
     st.x.copy_(X.view(T, cfg.layers, 1, spec.d))
     st.build_graph()
