@@ -178,6 +178,7 @@ WsLayout ws_layout(const pi_layer *L, int B) {
   w.count = off;   off += align_up(sizeof(int32_t) * 4);
   w.cnt = off;     off += align_up(sizeof(int32_t) * (size_t)step_grid(L));
   w.bar = off;     off += align_up(sizeof(unsigned));
+  w.abuf = off;    off += align_up(2 * sizeof(__half) * (size_t)tc_bpad(B) * tc_ffn_pad(L));
   w.total = off;
   return w;
 }
@@ -549,7 +550,7 @@ int32_t pi_forward_launches(const pi_layer *L, int32_t B) {
   if (!L || B < 1 || B > PI_MAX_BATCH) return 0;
   // B <= 2: one persistent cooperative launch (after a barrier-counter memset);
   // otherwise predict_h, predict_l, compact, up, down, reduce
-  return B <= 2 ? 1 : 6;
+  return B <= 2 ? 1 : 6;   // (tensor-core path: up, down, reduce; ALU path likewise)
 }
 
 pi_status pi_device_status(pi_layer *L, void *stream) {

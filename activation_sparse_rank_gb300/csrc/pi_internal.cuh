@@ -55,6 +55,7 @@ struct WsLayout {
   size_t count = 0;    // int32 [4]
   size_t cnt = 0;      // int32 [G]             per-CTA active counts (persistent step)
   size_t bar = 0;      // uint32                grid-barrier counter
+  size_t abuf = 0;     // fp16 [2*Bp, ffn_pad]  activations (hi; lo) of the tensor-core path
   size_t total = 0;
 };
 
@@ -130,6 +131,15 @@ cudaError_t run_compact(const pi_layer *L, const uint8_t *mask, int B, int32_t *
 cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                            const int32_t *count, int count_const, float *y,
                            const WsLayout &w, char *ws, cudaStream_t s);
+// Tensor-core (tcgen05) batched path for 3 <= B <= PI_MAX_BATCH (pi_tc.cu).
+bool tc_supported(const pi_layer *L, int B);
+int tc_bpad(int B);
+int tc_ffn_pad(const pi_layer *L);
+int tc_down_splits(const pi_layer *L);
+cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
+                              const int32_t *count, int count_const, float *y, const WsLayout &w,
+                              char *ws, cudaStream_t s);
+cudaError_t run_reduce(const float *partial, int nsplit, int n, float *y, cudaStream_t s);
 cudaError_t run_profile(const pi_layer_desc *desc, const __half *x, int T, int32_t *counts,
                         cudaStream_t s);
 

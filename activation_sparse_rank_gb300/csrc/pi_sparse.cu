@@ -395,9 +395,15 @@ int down_splits(const pi_layer *L, int B) {
   return n < 1 ? 1 : n;
 }
 
+cudaError_t run_reduce(const float *partial, int nsplit, int n, float *y, cudaStream_t s) {
+  const int n4 = n / 4;
+  return launch_pdl(k_reduce, dim3((n4 + 15) / 16), dim3(256), 0, s, partial, nsplit, n4, y);
+}
+
 cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                            const int32_t *count, int count_const, float *y, const WsLayout &w,
                            char *ws, cudaStream_t s) {
+  if (B > 2 && tc_supported(L, B)) return run_sparse_ffn_tc(L, x, B, idx, count, count_const, y, w, ws, s);
   float *partial = reinterpret_cast<float *>(ws + w.partial);
   const bool reglu = L->act == PI_ACT_REGLU;
   cudaError_t e;

@@ -1,0 +1,498 @@
+// Batched sparse FFN on the tensor cores (tcgen05, TMEM accumulators, TMA).
+//
+// "PowerInfer: Fast Large Language Model Serving with a Consumer-grade GPU"
+// (egguo-blog reading report), section 2.3 core module 4 (neuron-aware
+// operators) and section 4.4, limitation 3: with a batch of B tokens the
+// active set is the union over the batch, and the union's rows form a dense
+// contraction with the batch:
+//   up    H[u, b]  = W_up[idx[u], :] . x[b, :]           (and the gate rows)
+//         a[u, b]  = ReLU(H + bias)  or  ReLU(G + bias) * H
+//   down  y[b, j]  = sum_u a[u, b] W_down^T[idx[u], j]
+// Both products run as tcgen05.mma kind::f16 (fp16 operands, fp32 TMEM
+// accumulators).  The activations enter the second product as an fp16 pair
+// a = a_hi + a_lo (stacked as 2*Bp columns), which keeps their rounding error
+// near 2^-22 relative instead of fp16's 2^-11.
+//
+// k_tc_up:   persistent CTAs over 128-neuron tiles of the active list.  Per
+//            64-element K slab, TMA gathers the 128 rows (tile::gather4, 128B
+//            swizzle) and loads the x slab; one thread drives a multi-stage
+//            mbarrier pipeline and issues the MMAs; four warps read TMEM.
+// k_tc_down: CTA (column tile of 128, split of the list).  Per 64-neuron slab,
+//            TMA gathers 64 rows x 128 columns of W_down^T (MN-major operand)
+//            and loads the matching [a_hi; a_lo] slab; partial sums go to the
+//            workspace and k_reduce adds them in split order (deterministic).
+// All mbarrier waits are bounded; on a timeout the kernel sets a status bit,
+// waits (bounded) for its copies in flight, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "pi_internal.cuh"
+
+namespace {
+
+constexpr unsigned kSpin = 1u << 22;
+constexpr int kTile = 128;      // MMA M
+constexpr int kSlab = 64;       // K elements per slab (128 bytes of fp16)
+
+__device__ __forceinline__ uint32_t su32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool mb_wait(uint32_t mbar, uint32_t parity) {
+  for (unsigned it = 0; it < kSpin; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void mb_init(uint32_t mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count));
+}
+
+__device__ __forceinline__ void mb_expect(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, int r0, int r1, int r2,
+                                            int r3, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
+          dst),
+      "l"(map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout type 2).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with f16 A/B and f32 D.
+__device__ __forceinline__ uint32_t idesc_f16(int n, int m, bool a_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ int tmem_cols_for(int n) {
+  int c = 32;
+  while (c < n) c <<= 1;
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+template <bool REGLU>
+__global__ void __launch_bounds__(128, 1) k_tc_up(const __grid_constant__ CUtensorMap tm_g,   // gated rows (up / gate)
+                                                  const __grid_constant__ CUtensorMap tm_u,   // up rows (ReGLU)
+                                                  const __grid_constant__ CUtensorMap tm_x,
+                                                  const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
+                                                  int count_const, const float *__restrict__ bias, int d, int ffn,
+                                                  int B, int Bp, int nstage, __half *__restrict__ abuf, int abuf_ld,
+                                                  unsigned int *status) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  constexpr int NA = REGLU ? 2 : 1;
+  const uint32_t slabA = kTile * 128;                   // one gathered operand slab
+  const uint32_t slabX = (uint32_t)Bp * 128;
+  const uint32_t stage_bytes = NA * slabA + ((slabX + 1023) & ~1023u);
+  __shared__ __align__(8) unsigned long long full_s[8], empty_s[8], done_s;
+  __shared__ int rows_s[kTile];
+  __shared__ uint32_t taddr_s;
+  __shared__ int fail_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ncols = tmem_cols_for(NA * Bp);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mb_init(su32(&full_s[s]), 1);
+      mb_init(su32(&empty_s[s]), 1);
+    }
+    mb_init(su32(&done_s), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fail_s = 0;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = taddr_s;
+
+  int count = count_p ? *count_p : count_const;
+  if (count < 0 || count > ffn) {
+    if (tid == 0) atomicOr(status, PI_STATUS_BAD_COUNT);
+    count = count < 0 ? 0 : ffn;
+  }
+  const int ntiles = (count + kTile - 1) / kTile;
+  const int KT = d / kSlab;
+  const uint32_t idesc = idesc_f16(Bp, kTile, false);
+  uint32_t gslab = 0;          // slabs issued by this CTA so far (pipeline position)
+  uint32_t done_phase = 0;
+
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int k0 = tile * kTile;
+    {
+      const int k = k0 + tid;
+      int i = k < count ? (idx ? idx[k] : k) : -1;
+      if (k < count && (i < 0 || i >= ffn)) {
+        atomicOr(status, PI_STATUS_BAD_INDEX);
+        i = -2;
+      }
+      rows_s[tid] = i;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      // gather rows: invalid/padding rows read row 0 (their activation is written as 0)
+      auto row = [&](int q) { const int i = rows_s[q]; return i >= 0 ? i : 0; };
+      auto issue = [&](int kt, uint32_t g) {
+        const int s = (int)(g % (uint32_t)nstage);
+        if (g >= (uint32_t)nstage && !mb_wait(su32(&empty_s[s]), ((g / nstage) - 1) & 1)) fail_s = 1;
+        unsigned char *st = sm + (size_t)s * stage_bytes;
+        const uint32_t bar = su32(&full_s[s]);
+        mb_expect(bar, NA * slabA + slabX);
+        for (int q = 0; q < kTile; q += 4)
+          tma_gather4(su32(st + q * 128), &tm_g, kt * kSlab, row(q), row(q + 1), row(q + 2), row(q + 3), bar);
+        if (REGLU)
+          for (int q = 0; q < kTile; q += 4)
+            tma_gather4(su32(st + slabA + q * 128), &tm_u, kt * kSlab, row(q), row(q + 1), row(q + 2), row(q + 3), bar);
+        tma_tile2d(su32(st + NA * slabA), &tm_x, kt * kSlab, 0, bar);
+      };
+      const int pre = min(nstage - 1, KT);
+      for (int kt = 0; kt < pre; ++kt) issue(kt, gslab + kt);
+      for (int kt = 0; kt < KT && !fail_s; ++kt) {
+        const uint32_t g = gslab + kt;
+        if (kt + nstage - 1 < KT) issue(kt + nstage - 1, g + nstage - 1);
+        const int s = (int)(g % (uint32_t)nstage);
+        if (!mb_wait(su32(&full_s[s]), (g / nstage) & 1)) { fail_s = 1; break; }
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        unsigned char *st = sm + (size_t)s * stage_bytes;
+        const uint32_t xa = su32(st + NA * slabA);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
+          mma_f16(tmem, sdesc(su32(st) + kk * 32, 16, 1024), bd, idesc, (kt | kk) ? 1u : 0u);
+          if (REGLU) mma_f16(tmem + (uint32_t)Bp, sdesc(su32(st + slabA) + kk * 32, 16, 1024), bd, idesc, (kt | kk) ? 1u : 0u);
+        }
+        mma_commit(su32(&empty_s[s]));
+      }
+      gslab += KT;
+      mma_commit(su32(&done_s));
+    }
+    __syncthreads();
+    if (fail_s) break;
+    if (!mb_wait(su32(&done_s), done_phase)) { fail_s = 1; break; }
+    done_phase ^= 1u;
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    // epilogue: TMEM lane = tile row = warp*32 + lane
+    const int q = warp * 32 + lane;
+    const int i = rows_s[q];
+    const float bi = i >= 0 ? bias[i] : 0.f;
+    const int kq = k0 + q;
+    for (int c0 = 0; c0 < Bp; c0 += 8) {
+      float g8[8], u8[8];
+      tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, g8);
+      if (REGLU) tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(Bp + c0), u8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int b = c0 + j;
+        float a = 0.f;
+        if (i >= 0 && b < B) {
+          const float z = g8[j] + bi;
+          a = REGLU ? (z > 0.f ? z : 0.f) * u8[j] : (z > 0.f ? z : 0.f);
+        }
+        const __half hi = __float2half_rn(a);
+        const __half lo = __float2half_rn(a - __half2float(hi));
+        abuf[(size_t)b * abuf_ld + kq] = hi;
+        abuf[(size_t)(Bp + b) * abuf_ld + kq] = lo;
+      }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+  }
+  if (fail_s && tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
+  // let every copy issued by this CTA land before leaving (bounded)
+  if (tid == 0 && fail_s)
+    for (int s = 0; s < nstage; ++s) mb_wait(su32(&full_s[s]), 0), mb_wait(su32(&full_s[s]), 1);
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128, 1) k_tc_down(const __grid_constant__ CUtensorMap tm_w,   // W_down^T, box 64 x 1
+                                                    const __grid_constant__ CUtensorMap tm_a,   // abuf, box 64 x 2Bp
+                                                    const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
+                                                    int count_const, int d, int ffn, int B, int Bp, int nstage,
+                                                    float *__restrict__ partial, unsigned int *status) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  const int N2 = 2 * Bp;
+  const uint32_t half_bytes = kSlab * 128;                // 64 rows x 64 columns
+  const uint32_t slabW = 2 * half_bytes;                  // 128 columns
+  const uint32_t slabA = (uint32_t)N2 * 128;
+  const uint32_t stage_bytes = slabW + ((slabA + 1023) & ~1023u);
+  __shared__ __align__(8) unsigned long long full_s[8], empty_s[8], done_s;
+  __shared__ int rows_s[8][kSlab];
+  __shared__ uint32_t taddr_s;
+  __shared__ int fail_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j0 = blockIdx.x * kTile;
+  const int ncols = tmem_cols_for(N2);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mb_init(su32(&full_s[s]), 1);
+      mb_init(su32(&empty_s[s]), 1);
+    }
+    mb_init(su32(&done_s), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fail_s = 0;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = taddr_s;
+
+  int count = count_p ? *count_p : count_const;
+  if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;     // flagged by k_tc_up
+  const int KS = (count + kSlab - 1) / kSlab;
+  const int per = (KS + gridDim.y - 1) / gridDim.y;
+  const int ks0 = min(KS, (int)blockIdx.y * per), ks1 = min(KS, ks0 + per);
+  const int nk = ks1 - ks0;
+  const uint32_t idesc = idesc_f16(N2, kTile, true);
+
+  if (warp == 0 && nk > 0) {
+    // warp 0 drives the pipeline: its lanes fetch each slab's 64 row indices
+    // into shared memory, lane 0 issues the copies and the MMAs
+    auto issue = [&](int t) {
+      const int s = t % nstage;
+      if (t >= nstage && !mb_wait(su32(&empty_s[s]), ((t / nstage) - 1) & 1)) fail_s = 1;
+      const int slab = ks0 + t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int k = slab * kSlab + lane + 32 * h;
+        int i = k < count ? (idx ? idx[k] : k) : 0;
+        rows_s[s][lane + 32 * h] = (i >= 0 && i < ffn) ? i : 0;   // padding / invalid: row 0, zero activation
+      }
+      __syncwarp();
+      if (lane == 0) {
+        unsigned char *st = sm + (size_t)s * stage_bytes;
+        const uint32_t bar = su32(&full_s[s]);
+        mb_expect(bar, slabW + slabA);
+        for (int h = 0; h < 2; ++h)
+          for (int q = 0; q < kSlab; q += 4)
+            tma_gather4(su32(st + h * half_bytes + q * 128), &tm_w, j0 + h * 64, rows_s[s][q], rows_s[s][q + 1],
+                        rows_s[s][q + 2], rows_s[s][q + 3], bar);
+        tma_tile2d(su32(st + slabW), &tm_a, slab * kSlab, 0, bar);
+      }
+      __syncwarp();
+    };
+    const int pre = min(nstage - 1, nk);
+    for (int t = 0; t < pre; ++t) issue(t);
+    for (int t = 0; t < nk; ++t) {
+      if (fail_s) break;
+      if (t + nstage - 1 < nk) issue(t + nstage - 1);
+      const int s = t % nstage;
+      if (!mb_wait(su32(&full_s[s]), (t / nstage) & 1)) { fail_s = 1; break; }
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      if (lane == 0) {
+        unsigned char *st = sm + (size_t)s * stage_bytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // A: MN-major (K groups of 8 rows at 1024 B, column halves at half_bytes)
+          const uint64_t ad = sdesc(su32(st) + kk * 16 * 128, half_bytes, 1024);
+          const uint64_t bd = sdesc(su32(st + slabW) + kk * 32, 16, 1024);
+          mma_f16(tmem, ad, bd, idesc, (t | kk) ? 1u : 0u);
+        }
+        mma_commit(su32(&empty_s[s]));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(su32(&done_s));
+    __syncwarp();
+  }
+  __syncthreads();
+  const int j = j0 + warp * 32 + lane;               // TMEM lane = output column
+  if (nk > 0 && !fail_s) {
+    if (!mb_wait(su32(&done_s), 0)) fail_s = 1;
+  }
+  __syncthreads();
+  if (!fail_s) {
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    for (int c0 = 0; c0 < Bp; c0 += 8) {
+      float hi[8], lo[8];
+      if (nk > 0) {
+        tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, hi);
+        tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(Bp + c0), lo);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int b = c0 + q;
+        if (b < B && j < d) partial[((size_t)blockIdx.y * B + b) * d + j] = hi[q] + lo[q];
+      }
+    }
+  } else if (tid == 0) {
+    atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
+    for (int s = 0; s < nstage; ++s) mb_wait(su32(&full_s[s]), 0), mb_wait(su32(&full_s[s]), 1);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
+}
+
+// ---------------------------------------------------------------------------
+// The driver's tensor-map encoder, looked up through the runtime so that the
+// library does not link libcuda (it must load on machines without a driver).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer) {
+  const EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kTcSmemBudget = 200 * 1024;
+
+}  // namespace
+
+namespace pi {
+
+bool tc_supported(const pi_layer *L, int B) {
+  return B >= 3 && B <= PI_MAX_BATCH && L->d % kSlab == 0 && L->d >= kTile;
+}
+
+int tc_bpad(int B) { return (B + 15) & ~15; }   // MMA N: a multiple of 16
+
+int tc_ffn_pad(const pi_layer *L) { return (L->ffn + kTile - 1) / kTile * kTile; }
+
+int tc_down_splits(const pi_layer *L) {
+  const int tiles = L->d / kTile + (L->d % kTile ? 1 : 0);
+  int s = L->num_sms / tiles;
+  return s < 1 ? 1 : s;
+}
+
+cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
+                              const int32_t *count, int count_const, float *y, const WsLayout &w,
+                              char *ws, cudaStream_t s) {
+  const bool reglu = L->act == PI_ACT_REGLU;
+  const int Bp = tc_bpad(B);
+  const int ffn_pad = tc_ffn_pad(L);
+  __half *abuf = reinterpret_cast<__half *>(ws + w.abuf);
+  float *partial = reinterpret_cast<float *>(ws + w.partial);
+  CUtensorMap tm_g, tm_u, tm_x, tm_w, tm_a;
+  const uint64_t row_bytes = (uint64_t)L->d * 2;
+  if (!encode_2d(&tm_g, reglu ? L->W_gate : L->W_up, L->d, L->ffn, row_bytes, kSlab, 1) ||
+      !encode_2d(&tm_u, L->W_up, L->d, L->ffn, row_bytes, kSlab, 1) ||
+      !encode_2d(&tm_x, x, L->d, B, row_bytes, kSlab, Bp) ||
+      !encode_2d(&tm_w, L->W_dT, L->d, L->ffn, row_bytes, kSlab, 1) ||
+      !encode_2d(&tm_a, abuf, ffn_pad, 2 * Bp, (uint64_t)ffn_pad * 2, kSlab, 2 * Bp))
+    return cudaErrorInvalidValue;
+
+  // up: stages of (1 or 2) x 16 KB gathered rows + the x slab
+  const int NA = reglu ? 2 : 1;
+  const size_t up_stage = NA * (size_t)kTile * 128 + (((size_t)Bp * 128 + 1023) & ~(size_t)1023);
+  int up_ns = (int)((kTcSmemBudget - 1024) / up_stage);
+  if (up_ns > 8) up_ns = 8;
+  if (up_ns < 2) return cudaErrorInvalidValue;
+  const size_t up_smem = 1024 + up_ns * up_stage;
+  auto up = reglu ? k_tc_up<true> : k_tc_up<false>;
+  cudaError_t e = cudaFuncSetAttribute(up, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up_smem);
+  if (e != cudaSuccess) return e;
+  e = record_hook(L->ev_before, s);
+  if (e != cudaSuccess) return e;
+  int grid_up = (L->ffn + kTile - 1) / kTile;
+  if (grid_up > L->num_sms) grid_up = L->num_sms;
+  up<<<grid_up, 128, up_smem, s>>>(tm_g, tm_u, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B, Bp, up_ns,
+                                   abuf, ffn_pad, L->status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  // down: stages of 16 KB gathered W_down^T + the [a_hi; a_lo] slab
+  const size_t dn_stage = 2 * (size_t)kSlab * 128 + (((size_t)2 * Bp * 128 + 1023) & ~(size_t)1023);
+  int dn_ns = (int)((kTcSmemBudget - 1024) / dn_stage);
+  if (dn_ns > 8) dn_ns = 8;
+  if (dn_ns < 2) return cudaErrorInvalidValue;
+  const size_t dn_smem = 1024 + dn_ns * dn_stage;
+  e = cudaFuncSetAttribute(k_tc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
+  if (e != cudaSuccess) return e;
+  const int nsplit = tc_down_splits(L);
+  dim3 grid_dn(L->d / kTile + (L->d % kTile ? 1 : 0), nsplit);
+  k_tc_down<<<grid_dn, 128, dn_smem, s>>>(tm_w, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns, partial,
+                                         L->status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = record_hook(L->ev_after, s);
+  if (e != cudaSuccess) return e;
+  return run_reduce(partial, nsplit, B * L->d, y, s);
+}
+
+}  // namespace pi

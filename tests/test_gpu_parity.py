@@ -245,3 +245,30 @@ def test_profile_counts(pi):
     ce_ref, _ = O.profile_counts(Le, Xe)
     np.testing.assert_array_equal(ce, ce_ref)
     np.testing.assert_array_equal(pi.hot_first_perm(ce), O.hot_first_order(ce_ref))
+
+
+@pytest.mark.parametrize("act,d,ffn,r", [("relu", 4096, 6000, 256), ("reglu", 2048, 3000, 64),
+                                         ("relu", 12288, 1100, 128)])
+@pytest.mark.parametrize("B", [3, 8, 16, 32, 64, 128])
+def test_batched_tensor_core_path(pi, act, d, ffn, r, B):
+    """Batches of 3+ run the tcgen05 gathered-tile kernels: union set of the
+    batch, activations split into an fp16 pair; checked on every token."""
+    t, _ = _layer(LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1), seed=d + 7 * B)
+    layer = pi.Layer.from_dict(to_dev(t))
+    L = stored_oracle(layer, t)
+    x = make_tokens(d, B, seed=B)
+    h = O.predictor_hidden(L, x)
+    S = O.active_union(O.predicted_mask(O.predictor_logits(L, h)))
+    idx = torch.from_numpy(S.astype(np.int32)).cuda()
+    count = torch.tensor([S.size], dtype=torch.int32, device="cuda")
+    y = layer.sparse_ffn(x.cuda(), idx, count)
+    y2 = layer.sparse_ffn(x.cuda(), idx, count)
+    torch.cuda.synchronize()
+    rows = list(range(B)) if B <= 16 else [0, 1, B // 2, B - 1]
+    check_y(y.cpu().numpy()[rows], O.sparse_ffn(L, x[rows], S))
+    assert torch.equal(y, y2)
+    assert layer.device_status() == 0
+    if B in (8, 128) and act == "relu":
+        yd = layer.dense_ref(x.cuda())
+        torch.cuda.synchronize()
+        check_y(yd.cpu().numpy()[rows], O.dense_ffn(L, x[rows]))
