@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0, help="override tokens per step (debug)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=1,
+                    help="tokens per decode batch (the headline metric is batch 1)")
     return ap.parse_args()
 
 
@@ -264,12 +266,13 @@ def main():
     spec = cfg.layer
     n_layers = args.layers or cfg.layers
     T = args.tokens or cfg.tokens
-    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
+    Bt = args.batch
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1 and Bt == 1
     t_setup = time.perf_counter()
     layers, host_layers = build_stack(cfg, device, n_layers, keep_host_layers=2 if want_cpu else 0)
-    stack = SparseFFNStack(layers, tokens=T, B=1)
-    X = make_tokens(spec.d, T * n_layers, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
-    stack.x.copy_(X.view(T, n_layers, 1, spec.d))
+    stack = SparseFFNStack(layers, tokens=T, B=Bt)
+    X = make_tokens(spec.d, T * n_layers * Bt, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
+    stack.x.copy_(X.view(T, n_layers, Bt, spec.d))
     del X
     stack.build_graph()
     torch.cuda.synchronize()
@@ -307,7 +310,7 @@ def main():
         if layer.device_status() != 0:
             raise RuntimeError("device check failed during the timed steps")
 
-    tokens_step = T * 1
+    tokens_step = T * Bt
     value = tokens_step * world / (ms / 1000.0)
     tb = touched_bytes(cfg, stack.count)
     mean_S = float(stack.count.double().mean().item())
@@ -319,7 +322,7 @@ def main():
     Td = min(16, T)
     dense_g = torch.cuda.CUDAGraph()
     ws = stack.ws
-    yd = torch.empty(n_layers, 1, spec.d, dtype=torch.float32, device=device)
+    yd = torch.empty(n_layers, Bt, spec.d, dtype=torch.float32, device=device)
     with torch.cuda.stream(s):
         for li, layer in enumerate(layers):
             layer.dense_ref(stack.x[0, li], yd[li], ws=ws, stream=s)
@@ -339,7 +342,7 @@ def main():
             dense_g.replay()
     e1.record(s)
     torch.cuda.synchronize()
-    dense_tok_s = 3 * Td / (e0.elapsed_time(e1) / 1000.0)
+    dense_tok_s = 3 * Td * Bt / (e0.elapsed_time(e1) / 1000.0)
 
     # dominant kernel (the persistent step kernel, one launch per token)
     # timed inside a captured step with external event-record nodes
@@ -371,8 +374,13 @@ def main():
         how = "events around each launch, eager step"
     k_ms = [evs[t][0].elapsed_time(evs[t][1]) for t in range(Tr)]
     cnt = stack.count[:Tr].cpu().numpy()
-    alg_bytes = (Tr * n_layers * predictor_bytes(spec.d, spec.ffn, spec.rank)
-                 + float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act))
+    if Bt <= 2:   # the persistent step: predictor + rows of every layer
+        alg_bytes = (Tr * n_layers * predictor_bytes(spec.d, spec.ffn, spec.rank)
+                     + float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act))
+        kname = f"k_stack_step (one token through {n_layers} layers)"
+    else:         # tensor-core up + down of layer 0: its active rows
+        alg_bytes = float(cnt[:, 0].sum()) * bytes_per_active_neuron(spec.d, spec.act)
+        kname = "k_tc_up + k_tc_down (layer 0, tcgen05)"
     k_avg_ms = sum(k_ms) / len(k_ms)
     achieved = alg_bytes / len(k_ms) / (k_avg_ms / 1e3) / 1e9
     traffic = None
@@ -381,13 +389,19 @@ def main():
         tj = json.loads(tfile.read_text())
         if tj.get("kernel_source_hash") == kernel_source_hash():
             traffic = tj.get("bytes_per_launch")
+    if Bt > 2:
+        traffic = None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": f"k_stack_step (one token through {n_layers} layers)",
+                "kernel": kname,
                 "peak_kind": peak_kind + " (copy bandwidth)",
                 "launches_timed": len(k_ms), "avg_launch_us": k_avg_ms * 1e3,
                 "algorithmic_bytes_per_launch": alg_bytes / len(k_ms),
                 "timing": how}
+    if Bt > 2:
+        mult = 3 if spec.act == "reglu" else 2
+        flops = 2.0 * Bt * float(cnt[:, 0].sum()) * spec.d * mult / len(k_ms)
+        roofline["tensor_tflops"] = flops / (k_avg_ms / 1e3) / 1e12
 
     # end to end from pinned host buffers through the public API
     xh = torch.empty_like(stack.x, device="cpu").pin_memory()
@@ -424,7 +438,7 @@ def main():
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": cfg.description, "name": cfg.name, "d": spec.d,
                        "ffn": spec.ffn, "rank": spec.rank, "layers": n_layers,
-                       "tokens_per_step": T, "batch": 1, "act": spec.act,
+                       "tokens_per_step": T * Bt, "batch": Bt, "act": spec.act,
                        "weights": "fp16", "hot_first": bool(cfg.profile_tokens),
                        "l2": "inputs larger than L2: ~1.2 GB of distinct weight rows per step",
                        "parallelism": f"replicas{world}"},
