@@ -14,13 +14,17 @@
 // near 2^-22 relative instead of fp16's 2^-11.
 //
 // k_tc_up:   persistent CTAs over 128-neuron tiles of the active list.  Per
-//            64-element K slab, TMA gathers the 128 rows (tile::gather4, 128B
-//            swizzle) and loads the x slab; one thread drives a multi-stage
-//            mbarrier pipeline and issues the MMAs; four warps read TMEM.
+//            64-element K slab, all 128 threads gather the 128 rows with
+//            16-byte cp.async copies written straight into the 128-byte
+//            swizzled operand layout (a gathered row piece is only 128 bytes,
+//            too small for TMA to move at full rate), TMA loads the x slab,
+//            and thread 0 issues the MMAs of a multi-stage mbarrier pipeline;
+//            four warps then read the accumulators from TMEM.
 // k_tc_down: CTA (column tile of 128, split of the list).  Per 64-neuron slab,
-//            TMA gathers 64 rows x 128 columns of W_down^T (MN-major operand)
-//            and loads the matching [a_hi; a_lo] slab; partial sums go to the
-//            workspace and k_reduce adds them in split order (deterministic).
+//            the threads gather 64 rows x 128 columns of W_down^T (MN-major
+//            operand) the same way and TMA loads the matching [a_hi; a_lo]
+//            slab; partial sums go to the workspace and k_reduce adds them
+//            in split order (deterministic).
 // All mbarrier waits are bounded; on a timeout the kernel sets a status bit,
 // waits (bounded) for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
@@ -75,6 +79,18 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// 16-byte global -> shared copy (L2 only), and an mbarrier arrival once all of
+// this thread's earlier copies have landed (counted against the init count).
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_arrive(uint32_t mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(mbar) : "memory");
+}
+// Offset of 16-byte chunk c of row r in a 128-byte-swizzled tile of 128-byte rows
+// (the layout TMA writes with 128B swizzle and the MMA reads with layout type 2).
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout type 2).
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -120,8 +136,8 @@ __device__ __forceinline__ int tmem_cols_for(int n) {
 
 // ---------------------------------------------------------------------------
 template <bool REGLU>
-__global__ void __launch_bounds__(128, 1) k_tc_up(const __grid_constant__ CUtensorMap tm_g,   // gated rows (up / gate)
-                                                  const __grid_constant__ CUtensorMap tm_u,   // up rows (ReGLU)
+__global__ void __launch_bounds__(128, 1) k_tc_up(const __half *__restrict__ Wg,   // gated rows (up / gate)
+                                                  const __half *__restrict__ Wu,   // up rows (ReGLU)
                                                   const __grid_constant__ CUtensorMap tm_x,
                                                   const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
                                                   int count_const, const float *__restrict__ bias, int d, int ffn,
@@ -146,7 +162,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_up(const __grid_constant__ CUtens
   }
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
-      mb_init(su32(&full_s[s]), 1);
+      mb_init(su32(&full_s[s]), 129);   // 128 copy arrivals + the TMA expect_tx arrival
       mb_init(su32(&empty_s[s]), 1);
     }
     mb_init(su32(&done_s), 1);
@@ -181,42 +197,68 @@ __global__ void __launch_bounds__(128, 1) k_tc_up(const __grid_constant__ CUtens
       rows_s[tid] = i;
     }
     __syncthreads();
-    if (tid == 0) {
-      // gather rows: invalid/padding rows read row 0 (their activation is written as 0)
-      auto row = [&](int q) { const int i = rows_s[q]; return i >= 0 ? i : 0; };
+    {
+      // Every thread copies 8 of the 1024 16-byte chunks of each gathered
+      // slab (8 threads per 128-byte row piece, rows t/8 + 16 i), straight
+      // into the swizzled layout; thread 0 also loads the x slab by TMA and
+      // issues the MMAs.  Invalid / padding rows read row 0 (their
+      // activation is written as 0).
+      const int cch = tid & 7;
+      const __half *gsrc[8], *usrc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = (tid >> 3) + 16 * i;
+        const int rid = rows_s[q] >= 0 ? rows_s[q] : 0;
+        gsrc[i] = Wg + (size_t)rid * d + cch * 8;
+        usrc[i] = REGLU ? Wu + (size_t)rid * d + cch * 8 : nullptr;
+      }
       auto issue = [&](int kt, uint32_t g) {
         const int s = (int)(g % (uint32_t)nstage);
         if (g >= (uint32_t)nstage && !mb_wait(su32(&empty_s[s]), ((g / nstage) - 1) & 1)) fail_s = 1;
         unsigned char *st = sm + (size_t)s * stage_bytes;
         const uint32_t bar = su32(&full_s[s]);
-        mb_expect(bar, NA * slabA + slabX);
-        for (int q = 0; q < kTile; q += 4)
-          tma_gather4(su32(st + q * 128), &tm_g, kt * kSlab, row(q), row(q + 1), row(q + 2), row(q + 3), bar);
-        if (REGLU)
-          for (int q = 0; q < kTile; q += 4)
-            tma_gather4(su32(st + slabA + q * 128), &tm_u, kt * kSlab, row(q), row(q + 1), row(q + 2), row(q + 3), bar);
-        tma_tile2d(su32(st + NA * slabA), &tm_x, kt * kSlab, 0, bar);
+        const uint32_t base = su32(st);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int q = (tid >> 3) + 16 * i;
+          cp16(base + sw128(q, cch), gsrc[i] + kt * kSlab);
+          if (REGLU) cp16(base + slabA + sw128(q, cch), usrc[i] + kt * kSlab);
+        }
+        cp_arrive(bar);
+        if (tid == 0) {
+          mb_expect(bar, slabX);
+          tma_tile2d(su32(st + NA * slabA), &tm_x, kt * kSlab, 0, bar);
+        }
       };
       const int pre = min(nstage - 1, KT);
       for (int kt = 0; kt < pre; ++kt) issue(kt, gslab + kt);
-      for (int kt = 0; kt < KT && !fail_s; ++kt) {
+      for (int kt = 0; kt < KT; ++kt) {
+        if (fail_s) break;
         const uint32_t g = gslab + kt;
         if (kt + nstage - 1 < KT) issue(kt + nstage - 1, g + nstage - 1);
-        const int s = (int)(g % (uint32_t)nstage);
-        if (!mb_wait(su32(&full_s[s]), (g / nstage) & 1)) { fail_s = 1; break; }
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        unsigned char *st = sm + (size_t)s * stage_bytes;
-        const uint32_t xa = su32(st + NA * slabA);
+        if (tid == 0) {
+          const int s = (int)(g % (uint32_t)nstage);
+          if (!mb_wait(su32(&full_s[s]), (g / nstage) & 1)) {
+            fail_s = 1;
+          } else {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            unsigned char *st = sm + (size_t)s * stage_bytes;
+            const uint32_t xa = su32(st + NA * slabA);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
-          mma_f16(tmem, sdesc(su32(st) + kk * 32, 16, 1024), bd, idesc, (kt | kk) ? 1u : 0u);
-          if (REGLU) mma_f16(tmem + (uint32_t)Bp, sdesc(su32(st + slabA) + kk * 32, 16, 1024), bd, idesc, (kt | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
+              mma_f16(tmem, sdesc(su32(st) + kk * 32, 16, 1024), bd, idesc, (kt | kk) ? 1u : 0u);
+              if (REGLU)
+                mma_f16(tmem + (uint32_t)Bp, sdesc(su32(st + slabA) + kk * 32, 16, 1024), bd, idesc,
+                        (kt | kk) ? 1u : 0u);
+            }
+            mma_commit(su32(&empty_s[s]));
+          }
         }
-        mma_commit(su32(&empty_s[s]));
       }
       gslab += KT;
-      mma_commit(su32(&done_s));
+      if (tid == 0) mma_commit(su32(&done_s));
     }
     __syncthreads();
     if (fail_s) break;
@@ -259,7 +301,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_up(const __grid_constant__ CUtens
 }
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128, 1) k_tc_down(const __grid_constant__ CUtensorMap tm_w,   // W_down^T, box 64 x 1
+__global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ Wd,                  // W_down^T
                                                     const __grid_constant__ CUtensorMap tm_a,   // abuf, box 64 x 2Bp
                                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
                                                     int count_const, int d, int ffn, int B, int Bp, int nstage,
@@ -272,7 +314,6 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __grid_constant__ CUte
   const uint32_t slabA = (uint32_t)N2 * 128;
   const uint32_t stage_bytes = slabW + ((slabA + 1023) & ~1023u);
   __shared__ __align__(8) unsigned long long full_s[8], empty_s[8], done_s;
-  __shared__ int rows_s[8][kSlab];
   __shared__ uint32_t taddr_s;
   __shared__ int fail_s;
 
@@ -285,7 +326,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __grid_constant__ CUte
   }
   if (tid == 0) {
     for (int s = 0; s < nstage; ++s) {
-      mb_init(su32(&full_s[s]), 1);
+      mb_init(su32(&full_s[s]), 129);   // 128 copy arrivals + the TMA expect_tx arrival
       mb_init(su32(&empty_s[s]), 1);
     }
     mb_init(su32(&done_s), 1);
@@ -305,55 +346,60 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __grid_constant__ CUte
   const int nk = ks1 - ks0;
   const uint32_t idesc = idesc_f16(N2, kTile, true);
 
-  if (warp == 0 && nk > 0) {
-    // warp 0 drives the pipeline: its lanes fetch each slab's 64 row indices
-    // into shared memory, lane 0 issues the copies and the MMAs
+  if (nk > 0) {
+    // Every thread copies 16 of the 2048 16-byte chunks of a slab: chunk
+    // c = tid % 8 of column half (tid / 8) % 2 of rows tid / 16 + 8 i, into the
+    // MN-major swizzled layout (8 rows of 128 bytes per 1024-byte group);
+    // thread 0 also loads the [a_hi; a_lo] slab by TMA and issues the MMAs.
+    const int cch = tid & 7, hh = (tid >> 3) & 1, r0 = tid >> 4;
     auto issue = [&](int t) {
       const int s = t % nstage;
       if (t >= nstage && !mb_wait(su32(&empty_s[s]), ((t / nstage) - 1) & 1)) fail_s = 1;
+      unsigned char *st = sm + (size_t)s * stage_bytes;
+      const uint32_t bar = su32(&full_s[s]);
       const int slab = ks0 + t;
+      const uint32_t base = su32(st) + hh * half_bytes;
+      const int col = j0 + hh * 64 + cch * 8;
+      const int colc = col < d ? col : 0;            // a column past d reads column 0 (output dropped)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int k = slab * kSlab + lane + 32 * h;
-        int i = k < count ? (idx ? idx[k] : k) : 0;
-        rows_s[s][lane + 32 * h] = (i >= 0 && i < ffn) ? i : 0;   // padding / invalid: row 0, zero activation
+      for (int i = 0; i < 8; ++i) {
+        const int q = r0 + 8 * i;
+        const int k = slab * kSlab + q;
+        int rid = k < count ? (idx ? idx[k] : k) : 0;
+        rid = (rid >= 0 && rid < ffn) ? rid : 0;     // padding / invalid: row 0 times a zero activation
+        cp16(base + sw128(q, cch), Wd + (size_t)rid * d + colc);
       }
-      __syncwarp();
-      if (lane == 0) {
-        unsigned char *st = sm + (size_t)s * stage_bytes;
-        const uint32_t bar = su32(&full_s[s]);
-        mb_expect(bar, slabW + slabA);
-        for (int h = 0; h < 2; ++h)
-          for (int q = 0; q < kSlab; q += 4)
-            tma_gather4(su32(st + h * half_bytes + q * 128), &tm_w, j0 + h * 64, rows_s[s][q], rows_s[s][q + 1],
-                        rows_s[s][q + 2], rows_s[s][q + 3], bar);
+      cp_arrive(bar);
+      if (tid == 0) {
+        mb_expect(bar, slabA);
         tma_tile2d(su32(st + slabW), &tm_a, slab * kSlab, 0, bar);
       }
-      __syncwarp();
     };
     const int pre = min(nstage - 1, nk);
     for (int t = 0; t < pre; ++t) issue(t);
     for (int t = 0; t < nk; ++t) {
       if (fail_s) break;
       if (t + nstage - 1 < nk) issue(t + nstage - 1);
-      const int s = t % nstage;
-      if (!mb_wait(su32(&full_s[s]), (t / nstage) & 1)) { fail_s = 1; break; }
-      asm volatile("tcgen05.fence::after_thread_sync;");
-      if (lane == 0) {
-        unsigned char *st = sm + (size_t)s * stage_bytes;
+      if (tid == 0) {
+        const int s = t % nstage;
+        if (!mb_wait(su32(&full_s[s]), (t / nstage) & 1)) {
+          fail_s = 1;
+        } else {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          asm volatile("tcgen05.fence::after_thread_sync;");
+          unsigned char *st = sm + (size_t)s * stage_bytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // A: MN-major (K groups of 8 rows at 1024 B, column halves at half_bytes)
-          const uint64_t ad = sdesc(su32(st) + kk * 16 * 128, half_bytes, 1024);
-          const uint64_t bd = sdesc(su32(st + slabW) + kk * 32, 16, 1024);
-          mma_f16(tmem, ad, bd, idesc, (t | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: MN-major (K groups of 8 rows at 1024 B, column halves at half_bytes)
+            const uint64_t ad = sdesc(su32(st) + kk * 16 * 128, half_bytes, 1024);
+            const uint64_t bd = sdesc(su32(st + slabW) + kk * 32, 16, 1024);
+            mma_f16(tmem, ad, bd, idesc, (t | kk) ? 1u : 0u);
+          }
+          mma_commit(su32(&empty_s[s]));
         }
-        mma_commit(su32(&empty_s[s]));
       }
-      __syncwarp();
     }
-    if (lane == 0) mma_commit(su32(&done_s));
-    __syncwarp();
+    if (tid == 0) mma_commit(su32(&done_s));
   }
   __syncthreads();
   const int j = j0 + warp * 32 + lane;               // TMEM lane = output column
@@ -448,12 +494,9 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   const int ffn_pad = tc_ffn_pad(L);
   __half *abuf = reinterpret_cast<__half *>(ws + w.abuf);
   float *partial = reinterpret_cast<float *>(ws + w.partial);
-  CUtensorMap tm_g, tm_u, tm_x, tm_w, tm_a;
+  CUtensorMap tm_x, tm_a;
   const uint64_t row_bytes = (uint64_t)L->d * 2;
-  if (!encode_2d(&tm_g, reglu ? L->W_gate : L->W_up, L->d, L->ffn, row_bytes, kSlab, 1) ||
-      !encode_2d(&tm_u, L->W_up, L->d, L->ffn, row_bytes, kSlab, 1) ||
-      !encode_2d(&tm_x, x, L->d, B, row_bytes, kSlab, Bp) ||
-      !encode_2d(&tm_w, L->W_dT, L->d, L->ffn, row_bytes, kSlab, 1) ||
+  if (!encode_2d(&tm_x, x, L->d, B, row_bytes, kSlab, Bp) ||
       !encode_2d(&tm_a, abuf, ffn_pad, 2 * Bp, (uint64_t)ffn_pad * 2, kSlab, 2 * Bp))
     return cudaErrorInvalidValue;
 
@@ -471,8 +514,8 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   if (e != cudaSuccess) return e;
   int grid_up = (L->ffn + kTile - 1) / kTile;
   if (grid_up > L->num_sms) grid_up = L->num_sms;
-  up<<<grid_up, 128, up_smem, s>>>(tm_g, tm_u, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B, Bp, up_ns,
-                                   abuf, ffn_pad, L->status);
+  up<<<grid_up, 128, up_smem, s>>>(reglu ? L->W_gate : L->W_up, L->W_up, tm_x, idx, count, count_const, L->b,
+                                   L->d, L->ffn, B, Bp, up_ns, abuf, ffn_pad, L->status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -486,8 +529,8 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   if (e != cudaSuccess) return e;
   const int nsplit = tc_down_splits(L);
   dim3 grid_dn(L->d / kTile + (L->d % kTile ? 1 : 0), nsplit);
-  k_tc_down<<<grid_dn, 128, dn_smem, s>>>(tm_w, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns, partial,
-                                         L->status);
+  k_tc_down<<<grid_dn, 128, dn_smem, s>>>(L->W_dT, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns,
+                                         partial, L->status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = record_hook(L->ev_after, s);
