@@ -123,8 +123,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t record_hook(cudaEvent_t ev, cudaStream_t s);
 
 // Stage launchers (pi_predict.cu / pi_sparse.cu).  All asynchronous.
+// union_mask: mask is [ffn], 1 where any token of the batch is active
 cudaError_t run_predict(const pi_layer *L, const __half *x, int B, uint8_t *mask,
-                        float *logits, float *h_ws, cudaStream_t s);
+                        float *logits, float *h_ws, cudaStream_t s, bool union_mask = false);
 cudaError_t run_compact(const pi_layer *L, const uint8_t *mask, int B, int32_t *idx,
                         int32_t *count, cudaStream_t s);
 // idx == nullptr means the identity list 0..count_const-1 (count ignored).

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) k_predict_l(const __half *__restrict__ W_
                                                    const float *__restrict__ c_p,
                                                    const float *__restrict__ h, int B, int r,
                                                    int ffn, int G, uint8_t *__restrict__ mask,
-                                                   float *__restrict__ logits) {
+                                                   float *__restrict__ logits, int union_mask) {
   extern __shared__ float h_s[];   // [kBT, r]
   pidev::griddep_wait();
   pidev::griddep_launch();
@@ -110,7 +110,10 @@ __global__ void __launch_bounds__(256) k_predict_l(const __half *__restrict__ W_
         if (valid && sub == 0 && t < nb) {
           const float l = s + c_p[row];
           const size_t o = (size_t)(b0 + t) * ffn + row;
-          if (mask) mask[o] = l > 0.f ? 1 : 0;
+          if (mask) {
+            if (!union_mask) mask[o] = l > 0.f ? 1 : 0;
+            else if (l > 0.f) mask[row] = 1;      // OR over the batch (zeroed before the launch)
+          }
           if (logits) logits[o] = l;
         }
       }
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(1024) k_compact(const uint8_t *__restrict__ ma
 namespace pi {
 
 cudaError_t run_predict(const pi_layer *L, const __half *x, int B, uint8_t *mask, float *logits,
-                        float *h_ws, cudaStream_t s) {
+                        float *h_ws, cudaStream_t s, bool union_mask) {
   const int warps_h = 4;
   const int grid_h = (L->rank + warps_h - 1) / warps_h;
   cudaError_t e = launch_pdl(k_predict_h, dim3(grid_h), dim3(32 * warps_h), 0, s, L->W_p1, x, B,
@@ -212,8 +215,12 @@ cudaError_t run_predict(const pi_layer *L, const __half *x, int B, uint8_t *mask
     e = cudaFuncSetAttribute(k_predict_l, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  if (union_mask) {
+    e = cudaMemsetAsync(mask, 0, (size_t)L->ffn, s);
+    if (e != cudaSuccess) return e;
+  }
   return launch_pdl(k_predict_l, dim3(grid_l), dim3(256), smem, s, L->W_p2, L->c_p, h_ws, B,
-                    L->rank, L->ffn, G, mask, logits);
+                    L->rank, L->ffn, G, mask, logits, union_mask ? 1 : 0);
 }
 
 cudaError_t run_compact(const pi_layer *L, const uint8_t *mask, int B, int32_t *idx,

@@ -226,8 +226,8 @@ def run_reference(args, cfg):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.description, "name": cfg.name, "d": spec.d, "ffn": spec.ffn,
-                   "rank": spec.rank, "layers": cfg.layers, "batch": 1},
+        "config": workload_config(cfg, args.layers or cfg.layers, args.tokens or cfg.tokens, 1,
+                                  int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{tot_p} (token, layer) pairs of layers 0..{n_layers - 1}, "
                                    f"{tot_t:.1f} s, scaled to a {cfg.layers}-layer stack; numpy "
@@ -235,6 +235,26 @@ def run_reference(args, cfg):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg, n_layers: int, T: int, Bt: int, world: int) -> dict:
+    """The config object both arms print for one workload."""
+    spec = cfg.layer
+    return {"workload": cfg.description, "name": cfg.name, "d": spec.d, "ffn": spec.ffn,
+            "rank": spec.rank, "layers": n_layers, "tokens_per_step": T * Bt, "batch": Bt,
+            "act": spec.act, "weights": "fp16", "hot_first": bool(cfg.profile_tokens),
+            "l2": "inputs larger than L2: the distinct weight rows of a step exceed the 129 MB L2",
+            "parallelism": f"replicas{world}"}
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets a timed region)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def kernel_source_hash() -> str:
@@ -301,11 +321,7 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, device=device)
     for layer in layers:
         if layer.device_status() != 0:
             raise RuntimeError("device check failed during the timed steps")
@@ -436,12 +452,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": cfg.description, "name": cfg.name, "d": spec.d,
-                       "ffn": spec.ffn, "rank": spec.rank, "layers": n_layers,
-                       "tokens_per_step": T * Bt, "batch": Bt, "act": spec.act,
-                       "weights": "fp16", "hot_first": bool(cfg.profile_tokens),
-                       "l2": "inputs larger than L2: ~1.2 GB of distinct weight rows per step",
-                       "parallelism": f"replicas{world}"},
+            "config": workload_config(cfg, n_layers, T, Bt, world),
             "effective_hbm_gbs": eff_gbs,
             "effective_frac_of_measured": eff_gbs / peak,
             "effective_frac_of_nominal_8tbs": eff_gbs / (NOMINAL_HBM_GBS),
