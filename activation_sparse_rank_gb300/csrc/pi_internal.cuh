@@ -56,6 +56,7 @@ struct WsLayout {
   size_t cnt = 0;      // int32 [G]             per-CTA active counts (persistent step)
   size_t bar = 0;      // uint32                grid-barrier counter
   size_t abuf = 0;     // fp16 [2*Bp, ffn_pad]  activations (hi; lo) of the tensor-core path
+  size_t hbuf = 0;     // fp16 [2*Bp, rank_pad] predictor hidden layer (hi; lo), tensor-core path
   size_t total = 0;
 };
 
@@ -137,6 +138,11 @@ bool tc_supported(const pi_layer *L, int B);
 int tc_bpad(int B);
 int tc_ffn_pad(const pi_layer *L);
 int tc_down_splits(const pi_layer *L);
+bool tc_predict_supported(const pi_layer *L, int B);
+int tc_rank_pad(const pi_layer *L);
+// h (fp16 pair, in hbuf [2Bp, rank_pad]) and the batch-union mask [ffn] on the tensor cores
+cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
+                           cudaStream_t s);
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,
                               char *ws, cudaStream_t s);

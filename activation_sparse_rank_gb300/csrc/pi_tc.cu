@@ -135,19 +135,30 @@ __device__ __forceinline__ int tmem_cols_for(int n) {
 }
 
 // ---------------------------------------------------------------------------
-template <bool REGLU>
-__global__ void __launch_bounds__(128, 1) k_tc_up(const __half *__restrict__ Wg,   // gated rows (up / gate)
-                                                  const __half *__restrict__ Wu,   // up rows (ReGLU)
-                                                  const __grid_constant__ CUtensorMap tm_x,
-                                                  const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
-                                                  int count_const, const float *__restrict__ bias, int d, int ffn,
-                                                  int B, int Bp, int nstage, __half *__restrict__ abuf, int abuf_ld,
-                                                  unsigned int *status) {
+// Row-tile GEMM D[128 rows, N] = W[rows, 0:K] . Bop[0:N, 0:K]^T with one of
+// three epilogues:
+//   kAct     a = ReLU(D + bias) (ReGLU: ReLU(D_gate + bias) * D_up), written
+//            as the fp16 pair (hi; lo) into out [2Bp, ld] (the sparse FFN up)
+//   kHidden  h = ReLU(D), written as the pair into out (predictor layer 1)
+//   kLogits  l = D_hi + D_lo + bias over the pair columns of Bop; mask[row] =
+//            1 if l > 0 for some token of the batch (predictor layer 2)
+constexpr int kAct = 0, kHidden = 1, kLogits = 2;
+
+template <int MODE, bool REGLU>
+__global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ Wg,   // rows (gated rows for kAct)
+                                                    const __half *__restrict__ Wu,   // up rows (ReGLU)
+                                                    const __grid_constant__ CUtensorMap tm_x,   // B operand
+                                                    const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
+                                                    int count_const, const float *__restrict__ bias, int d, int ffn,
+                                                    int B, int Bp, int nstage, __half *__restrict__ abuf, int abuf_ld,
+                                                    uint8_t *__restrict__ mask_out, unsigned int *status) {
+  // d: row length and contraction length K; ffn: number of rows of W
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   constexpr int NA = REGLU ? 2 : 1;
+  const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const uint32_t slabA = kTile * 128;                   // one gathered operand slab
-  const uint32_t slabX = (uint32_t)Bp * 128;
+  const uint32_t slabX = (uint32_t)Nmma * 128;
   const uint32_t stage_bytes = NA * slabA + ((slabX + 1023) & ~1023u);
   __shared__ __align__(8) unsigned long long full_s[8], empty_s[8], done_s;
   __shared__ int rows_s[kTile];
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_up(const __half *__restrict__ Wg,
   __shared__ int fail_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ncols = tmem_cols_for(NA * Bp);
+  const int ncols = tmem_cols_for(NA * Nmma);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -181,7 +192,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_up(const __half *__restrict__ Wg,
   }
   const int ntiles = (count + kTile - 1) / kTile;
   const int KT = d / kSlab;
-  const uint32_t idesc = idesc_f16(Bp, kTile, false);
+  const uint32_t idesc = idesc_f16(Nmma, kTile, false);
   uint32_t gslab = 0;          // slabs issued by this CTA so far (pipeline position)
   uint32_t done_phase = 0;
 
@@ -250,7 +261,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_up(const __half *__restrict__ Wg,
               const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
               mma_f16(tmem, sdesc(su32(st) + kk * 32, 16, 1024), bd, idesc, (kt | kk) ? 1u : 0u);
               if (REGLU)
-                mma_f16(tmem + (uint32_t)Bp, sdesc(su32(st + slabA) + kk * 32, 16, 1024), bd, idesc,
+                mma_f16(tmem + (uint32_t)Nmma, sdesc(su32(st + slabA) + kk * 32, 16, 1024), bd, idesc,
                         (kt | kk) ? 1u : 0u);
             }
             mma_commit(su32(&empty_s[s]));
@@ -268,24 +279,38 @@ __global__ void __launch_bounds__(128, 1) k_tc_up(const __half *__restrict__ Wg,
     // epilogue: TMEM lane = tile row = warp*32 + lane
     const int q = warp * 32 + lane;
     const int i = rows_s[q];
-    const float bi = i >= 0 ? bias[i] : 0.f;
+    const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
     const int kq = k0 + q;
-    for (int c0 = 0; c0 < Bp; c0 += 8) {
-      float g8[8], u8[8];
-      tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, g8);
-      if (REGLU) tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(Bp + c0), u8);
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    if (MODE == kLogits) {
+      bool on = false;
+      for (int c0 = 0; c0 < Bp; c0 += 8) {
+        float hi8[8], lo8[8];
+        tmem_ld8(trow + (uint32_t)c0, hi8);
+        tmem_ld8(trow + (uint32_t)(Bp + c0), lo8);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int b = c0 + j;
-        float a = 0.f;
-        if (i >= 0 && b < B) {
-          const float z = g8[j] + bi;
-          a = REGLU ? (z > 0.f ? z : 0.f) * u8[j] : (z > 0.f ? z : 0.f);
+        for (int j = 0; j < 8; ++j)
+          if (c0 + j < B) on |= (hi8[j] + lo8[j] + bi) > 0.f;
+      }
+      if (i >= 0) mask_out[i] = on ? 1 : 0;
+    } else {
+      for (int c0 = 0; c0 < Bp; c0 += 8) {
+        float g8[8], u8[8];
+        tmem_ld8(trow + (uint32_t)c0, g8);
+        if (REGLU) tmem_ld8(trow + (uint32_t)(Bp + c0), u8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int b = c0 + j;
+          float a = 0.f;
+          if (i >= 0 && b < B) {
+            const float z = g8[j] + bi;
+            a = REGLU ? (z > 0.f ? z : 0.f) * u8[j] : (z > 0.f ? z : 0.f);
+          }
+          const __half hi = __float2half_rn(a);
+          const __half lo = __float2half_rn(a - __half2float(hi));
+          abuf[(size_t)b * abuf_ld + kq] = hi;
+          abuf[(size_t)(Bp + b) * abuf_ld + kq] = lo;
         }
-        const __half hi = __float2half_rn(a);
-        const __half lo = __float2half_rn(a - __half2float(hi));
-        abuf[(size_t)b * abuf_ld + kq] = hi;
-        abuf[(size_t)(Bp + b) * abuf_ld + kq] = lo;
       }
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
@@ -352,6 +377,18 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
     // MN-major swizzled layout (8 rows of 128 bytes per 1024-byte group);
     // thread 0 also loads the [a_hi; a_lo] slab by TMA and issues the MMAs.
     const int cch = tid & 7, hh = (tid >> 3) & 1, r0 = tid >> 4;
+    // row indices of the next slab to issue, loaded one issue ahead so their
+    // latency hides behind the copies of the current slab
+    int nxt[8];
+    auto load_rows = [&](int slab) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = slab * kSlab + r0 + 8 * i;
+        int rid = k < count ? (idx ? idx[k] : k) : 0;
+        nxt[i] = (rid >= 0 && rid < ffn) ? rid : 0;  // padding / invalid: row 0 times a zero activation
+      }
+    };
+    load_rows(ks0);
     auto issue = [&](int t) {
       const int s = t % nstage;
       if (t >= nstage && !mb_wait(su32(&empty_s[s]), ((t / nstage) - 1) & 1)) fail_s = 1;
@@ -361,13 +398,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
       const uint32_t base = su32(st) + hh * half_bytes;
       const int col = j0 + hh * 64 + cch * 8;
       const int colc = col < d ? col : 0;            // a column past d reads column 0 (output dropped)
+      int cur[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+      if (t + 1 < nk) load_rows(slab + 1);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int q = r0 + 8 * i;
-        const int k = slab * kSlab + q;
-        int rid = k < count ? (idx ? idx[k] : k) : 0;
-        rid = (rid >= 0 && rid < ffn) ? rid : 0;     // padding / invalid: row 0 times a zero activation
-        cp16(base + sw128(q, cch), Wd + (size_t)rid * d + colc);
+        cp16(base + sw128(q, cch), Wd + (size_t)cur[i] * d + colc);
       }
       cp_arrive(bar);
       if (tid == 0) {
@@ -468,6 +506,27 @@ bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
 
 constexpr size_t kTcSmemBudget = 200 * 1024;
 
+template <int MODE, bool REGLU>
+cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, const CUtensorMap &tm_x,
+                        const int32_t *idx, const int32_t *count, int count_const, const float *bias, int K,
+                        int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, cudaStream_t s) {
+  const int NA = REGLU ? 2 : 1;
+  const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
+  const size_t stage = NA * (size_t)kTile * 128 + (((size_t)Nmma * 128 + 1023) & ~(size_t)1023);
+  int ns = (int)((kTcSmemBudget - 1024) / stage);
+  if (ns > 8) ns = 8;
+  if (ns < 2) return cudaErrorInvalidValue;
+  const size_t smem = 1024 + ns * stage;
+  auto kern = k_tc_rows<MODE, REGLU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = (nrows + kTile - 1) / kTile;
+  if (grid > L->num_sms) grid = L->num_sms;
+  kern<<<grid, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, out, out_ld, mask,
+                               L->status);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 namespace pi {
@@ -479,6 +538,28 @@ bool tc_supported(const pi_layer *L, int B) {
 int tc_bpad(int B) { return (B + 15) & ~15; }   // MMA N: a multiple of 16
 
 int tc_ffn_pad(const pi_layer *L) { return (L->ffn + kTile - 1) / kTile * kTile; }
+
+bool tc_predict_supported(const pi_layer *L, int B) {
+  return tc_supported(L, B) && L->rank % kSlab == 0;
+}
+
+int tc_rank_pad(const pi_layer *L) { return (L->rank + kTile - 1) / kTile * kTile; }
+
+cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
+                           cudaStream_t s) {
+  const int Bp = tc_bpad(B);
+  const int rpad = tc_rank_pad(L);
+  CUtensorMap tm_x, tm_h;
+  if (!encode_2d(&tm_x, x, L->d, B, (uint64_t)L->d * 2, kSlab, Bp) ||
+      !encode_2d(&tm_h, hbuf, rpad, 2 * Bp, (uint64_t)rpad * 2, kSlab, 2 * Bp))
+    return cudaErrorInvalidValue;
+  // h = ReLU(W_p1 x) as an fp16 pair, then l = W_p2 h + c_p -> union mask
+  cudaError_t e = launch_rows<kHidden, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr, L->d,
+                                              L->rank, B, Bp, hbuf, rpad, nullptr, s);
+  if (e != cudaSuccess) return e;
+  return launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->ffn, B,
+                                     Bp, nullptr, 0, mask_union, s);
+}
 
 int tc_down_splits(const pi_layer *L) {
   const int tiles = L->d / kTile + (L->d % kTile ? 1 : 0);
@@ -500,23 +581,12 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
       !encode_2d(&tm_a, abuf, ffn_pad, 2 * Bp, (uint64_t)ffn_pad * 2, kSlab, 2 * Bp))
     return cudaErrorInvalidValue;
 
-  // up: stages of (1 or 2) x 16 KB gathered rows + the x slab
-  const int NA = reglu ? 2 : 1;
-  const size_t up_stage = NA * (size_t)kTile * 128 + (((size_t)Bp * 128 + 1023) & ~(size_t)1023);
-  int up_ns = (int)((kTcSmemBudget - 1024) / up_stage);
-  if (up_ns > 8) up_ns = 8;
-  if (up_ns < 2) return cudaErrorInvalidValue;
-  const size_t up_smem = 1024 + up_ns * up_stage;
-  auto up = reglu ? k_tc_up<true> : k_tc_up<false>;
-  cudaError_t e = cudaFuncSetAttribute(up, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up_smem);
+  cudaError_t e = record_hook(L->ev_before, s);
   if (e != cudaSuccess) return e;
-  e = record_hook(L->ev_before, s);
-  if (e != cudaSuccess) return e;
-  int grid_up = (L->ffn + kTile - 1) / kTile;
-  if (grid_up > L->num_sms) grid_up = L->num_sms;
-  up<<<grid_up, 128, up_smem, s>>>(reglu ? L->W_gate : L->W_up, L->W_up, tm_x, idx, count, count_const, L->b,
-                                   L->d, L->ffn, B, Bp, up_ns, abuf, ffn_pad, L->status);
-  e = cudaGetLastError();
+  e = reglu ? launch_rows<kAct, true>(L, reglu ? L->W_gate : L->W_up, L->W_up, tm_x, idx, count, count_const, L->b,
+                                      L->d, L->ffn, B, Bp, abuf, ffn_pad, nullptr, s)
+            : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
+                                       Bp, abuf, ffn_pad, nullptr, s);
   if (e != cudaSuccess) return e;
 
   // down: stages of 16 KB gathered W_down^T + the [a_hi; a_lo] slab
