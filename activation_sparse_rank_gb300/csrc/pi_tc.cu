@@ -150,16 +150,19 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
                                                     const __grid_constant__ CUtensorMap tm_x,   // B operand
                                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
                                                     int count_const, const float *__restrict__ bias, int d, int ffn,
-                                                    int B, int Bp, int nstage, __half *__restrict__ abuf, int abuf_ld,
-                                                    uint8_t *__restrict__ mask_out, unsigned int *status) {
-  // d: row length and contraction length K; ffn: number of rows of W
+                                                    int B, int Bp, int nstage, int kw, __half *__restrict__ abuf,
+                                                    int abuf_ld, uint8_t *__restrict__ mask_out, unsigned int *status) {
+  // d: row length and contraction length K; ffn: number of rows of W.  A
+  // pipeline stage holds kw consecutive 64-element K slabs, so every gathered
+  // row contributes kw * 128 contiguous bytes per stage.
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   constexpr int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const uint32_t slabA = kTile * 128;                   // one gathered operand slab
   const uint32_t slabX = (uint32_t)Nmma * 128;
-  const uint32_t stage_bytes = NA * slabA + ((slabX + 1023) & ~1023u);
+  const uint32_t subX = (slabX + 1023) & ~1023u;
+  const uint32_t stage_bytes = (uint32_t)kw * (NA * slabA + subX);
   __shared__ __align__(8) unsigned long long full_s[8], empty_s[8], done_s;
   __shared__ int rows_s[kTile];
   __shared__ uint32_t taddr_s;
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
     count = count < 0 ? 0 : ffn;
   }
   const int ntiles = (count + kTile - 1) / kTile;
-  const int KT = d / kSlab;
+  const int KT = d / (kSlab * kw);
   const uint32_t idesc = idesc_f16(Nmma, kTile, false);
   uint32_t gslab = 0;          // slabs issued by this CTA so far (pipeline position)
   uint32_t done_phase = 0;
@@ -229,16 +232,20 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
         unsigned char *st = sm + (size_t)s * stage_bytes;
         const uint32_t bar = su32(&full_s[s]);
         const uint32_t base = su32(st);
+        for (int j = 0; j < kw; ++j) {
+          const int k0e = (kt * kw + j) * kSlab;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int q = (tid >> 3) + 16 * i;
-          cp16(base + sw128(q, cch), gsrc[i] + kt * kSlab);
-          if (REGLU) cp16(base + slabA + sw128(q, cch), usrc[i] + kt * kSlab);
+          for (int i = 0; i < 8; ++i) {
+            const int q = (tid >> 3) + 16 * i;
+            cp16(base + j * slabA + sw128(q, cch), gsrc[i] + k0e);
+            if (REGLU) cp16(base + (kw + j) * slabA + sw128(q, cch), usrc[i] + k0e);
+          }
         }
         cp_arrive(bar);
         if (tid == 0) {
-          mb_expect(bar, slabX);
-          tma_tile2d(su32(st + NA * slabA), &tm_x, kt * kSlab, 0, bar);
+          mb_expect(bar, kw * slabX);
+          for (int j = 0; j < kw; ++j)
+            tma_tile2d(su32(st + NA * kw * slabA + j * subX), &tm_x, (kt * kw + j) * kSlab, 0, bar);
         }
       };
       const int pre = min(nstage - 1, KT);
@@ -255,14 +262,17 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             asm volatile("tcgen05.fence::after_thread_sync;");
             unsigned char *st = sm + (size_t)s * stage_bytes;
-            const uint32_t xa = su32(st + NA * slabA);
+            for (int j = 0; j < kw; ++j) {
+              const uint32_t xa = su32(st + NA * kw * slabA + j * subX);
+              const uint32_t aa = su32(st + j * slabA);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
-              mma_f16(tmem, sdesc(su32(st) + kk * 32, 16, 1024), bd, idesc, (kt | kk) ? 1u : 0u);
-              if (REGLU)
-                mma_f16(tmem + (uint32_t)Nmma, sdesc(su32(st + slabA) + kk * 32, 16, 1024), bd, idesc,
-                        (kt | kk) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
+                const uint32_t acc = (kt | j | kk) ? 1u : 0u;
+                mma_f16(tmem, sdesc(aa + kk * 32, 16, 1024), bd, idesc, acc);
+                if (REGLU)
+                  mma_f16(tmem + (uint32_t)Nmma, sdesc(aa + kw * slabA + kk * 32, 16, 1024), bd, idesc, acc);
+              }
             }
             mma_commit(su32(&empty_s[s]));
           }
@@ -512,7 +522,11 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
                         int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, cudaStream_t s) {
   const int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
-  const size_t stage = NA * (size_t)kTile * 128 + (((size_t)Nmma * 128 + 1023) & ~(size_t)1023);
+  const size_t sub = NA * (size_t)kTile * 128 + (((size_t)Nmma * 128 + 1023) & ~(size_t)1023);
+  // widest stage (kw consecutive slabs per row) that divides K and keeps >= 2 stages
+  int kw = 4;
+  while (kw > 1 && ((K / kSlab) % kw != 0 || (kTcSmemBudget - 1024) / (kw * sub) < 2)) kw >>= 1;
+  const size_t stage = kw * sub;
   int ns = (int)((kTcSmemBudget - 1024) / stage);
   if (ns > 8) ns = 8;
   if (ns < 2) return cudaErrorInvalidValue;
@@ -522,8 +536,8 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   if (e != cudaSuccess) return e;
   int grid = (nrows + kTile - 1) / kTile;
   if (grid > L->num_sms) grid = L->num_sms;
-  kern<<<grid, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, out, out_ld, mask,
-                               L->status);
+  kern<<<grid, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, kw, out, out_ld,
+                               mask, L->status);
   return cudaGetLastError();
 }
 
