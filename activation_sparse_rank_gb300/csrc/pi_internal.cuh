@@ -137,7 +137,6 @@ cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int3
 bool tc_supported(const pi_layer *L, int B);
 int tc_bpad(int B);
 int tc_ffn_pad(const pi_layer *L);
-int tc_down_splits(const pi_layer *L);
 bool tc_predict_supported(const pi_layer *L, int B);
 int tc_rank_pad(const pi_layer *L);
 // h (fp16 pair, in hbuf [2Bp, rank_pad]) and the batch-union mask [ffn] on the tensor cores

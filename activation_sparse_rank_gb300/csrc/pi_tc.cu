@@ -340,12 +340,15 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
                                                     const __grid_constant__ CUtensorMap tm_a,   // abuf, box 64 x 2Bp
                                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
                                                     int count_const, int d, int ffn, int B, int Bp, int nstage,
-                                                    float *__restrict__ partial, unsigned int *status) {
+                                                    int cw, float *__restrict__ partial, unsigned int *status) {
+  // A CTA owns cw column tiles of 128 (cw * 256 contiguous bytes of every
+  // gathered W_down^T row per slab), one TMEM accumulator per tile.
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   const int N2 = 2 * Bp;
   const uint32_t half_bytes = kSlab * 128;                // 64 rows x 64 columns
-  const uint32_t slabW = 2 * half_bytes;                  // 128 columns
+  const uint32_t tileW = 2 * half_bytes;                  // 128 columns
+  const uint32_t slabW = (uint32_t)cw * tileW;
   const uint32_t slabA = (uint32_t)N2 * 128;
   const uint32_t stage_bytes = slabW + ((slabA + 1023) & ~1023u);
   __shared__ __align__(8) unsigned long long full_s[8], empty_s[8], done_s;
@@ -353,8 +356,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
   __shared__ int fail_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j0 = blockIdx.x * kTile;
-  const int ncols = tmem_cols_for(N2);
+  const int j0 = blockIdx.x * kTile * cw;
+  const int ncols = tmem_cols_for(cw * N2);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -405,17 +408,19 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
       unsigned char *st = sm + (size_t)s * stage_bytes;
       const uint32_t bar = su32(&full_s[s]);
       const int slab = ks0 + t;
-      const uint32_t base = su32(st) + hh * half_bytes;
-      const int col = j0 + hh * 64 + cch * 8;
-      const int colc = col < d ? col : 0;            // a column past d reads column 0 (output dropped)
       int cur[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
       if (t + 1 < nk) load_rows(slab + 1);
+      for (int c = 0; c < cw; ++c) {
+        const uint32_t base = su32(st) + c * tileW + hh * half_bytes;
+        const int col = j0 + c * kTile + hh * 64 + cch * 8;
+        const int colc = col < d ? col : 0;          // a column past d reads column 0 (output dropped)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int q = r0 + 8 * i;
-        cp16(base + sw128(q, cch), Wd + (size_t)cur[i] * d + colc);
+        for (int i = 0; i < 8; ++i) {
+          const int q = r0 + 8 * i;
+          cp16(base + sw128(q, cch), Wd + (size_t)cur[i] * d + colc);
+        }
       }
       cp_arrive(bar);
       if (tid == 0) {
@@ -436,13 +441,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           asm volatile("tcgen05.fence::after_thread_sync;");
           unsigned char *st = sm + (size_t)s * stage_bytes;
+          for (int c = 0; c < cw; ++c)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // A: MN-major (K groups of 8 rows at 1024 B, column halves at half_bytes)
-            const uint64_t ad = sdesc(su32(st) + kk * 16 * 128, half_bytes, 1024);
-            const uint64_t bd = sdesc(su32(st + slabW) + kk * 32, 16, 1024);
-            mma_f16(tmem, ad, bd, idesc, (t | kk) ? 1u : 0u);
-          }
+            for (int kk = 0; kk < 4; ++kk) {
+              // A: MN-major (K groups of 8 rows at 1024 B, column halves at half_bytes)
+              const uint64_t ad = sdesc(su32(st) + c * tileW + kk * 16 * 128, half_bytes, 1024);
+              const uint64_t bd = sdesc(su32(st + slabW) + kk * 32, 16, 1024);
+              mma_f16(tmem + (uint32_t)(c * N2), ad, bd, idesc, (t | kk) ? 1u : 0u);
+            }
           mma_commit(su32(&empty_s[s]));
         }
       }
@@ -450,26 +456,29 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
     if (tid == 0) mma_commit(su32(&done_s));
   }
   __syncthreads();
-  const int j = j0 + warp * 32 + lane;               // TMEM lane = output column
   if (nk > 0 && !fail_s) {
     if (!mb_wait(su32(&done_s), 0)) fail_s = 1;
   }
   __syncthreads();
   if (!fail_s) {
     asm volatile("tcgen05.fence::after_thread_sync;");
-    for (int c0 = 0; c0 < Bp; c0 += 8) {
-      float hi[8], lo[8];
-      if (nk > 0) {
-        tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, hi);
-        tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(Bp + c0), lo);
-      } else {
+    for (int c = 0; c < cw; ++c) {
+      const int j = j0 + c * kTile + warp * 32 + lane;   // TMEM lane = output column
+      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * N2);
+      for (int c0 = 0; c0 < Bp; c0 += 8) {
+        float hi[8], lo[8];
+        if (nk > 0) {
+          tmem_ld8(trow + (uint32_t)c0, hi);
+          tmem_ld8(trow + (uint32_t)(Bp + c0), lo);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.f;
-      }
+          for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.f;
+        }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int b = c0 + q;
-        if (b < B && j < d) partial[((size_t)blockIdx.y * B + b) * d + j] = hi[q] + lo[q];
+        for (int q = 0; q < 8; ++q) {
+          const int b = c0 + q;
+          if (b < B && j < d) partial[((size_t)blockIdx.y * B + b) * d + j] = hi[q] + lo[q];
+        }
       }
     }
   } else if (tid == 0) {
@@ -575,11 +584,7 @@ cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *m
                                      Bp, nullptr, 0, mask_union, s);
 }
 
-int tc_down_splits(const pi_layer *L) {
-  const int tiles = L->d / kTile + (L->d % kTile ? 1 : 0);
-  int s = L->num_sms / tiles;
-  return s < 1 ? 1 : s;
-}
+
 
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,
@@ -603,17 +608,20 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
                                        Bp, abuf, ffn_pad, nullptr, s);
   if (e != cudaSuccess) return e;
 
-  // down: stages of 16 KB gathered W_down^T + the [a_hi; a_lo] slab
-  const size_t dn_stage = 2 * (size_t)kSlab * 128 + (((size_t)2 * Bp * 128 + 1023) & ~(size_t)1023);
+  // down: stages of cw x 16 KB gathered W_down^T + the [a_hi; a_lo] slab
+  const int cw = (L->d % (2 * kTile) == 0 && 2 * 2 * Bp <= 512) ? 2 : 1;
+  const size_t dn_stage = cw * 2 * (size_t)kSlab * 128 + (((size_t)2 * Bp * 128 + 1023) & ~(size_t)1023);
   int dn_ns = (int)((kTcSmemBudget - 1024) / dn_stage);
   if (dn_ns > 8) dn_ns = 8;
   if (dn_ns < 2) return cudaErrorInvalidValue;
   const size_t dn_smem = 1024 + dn_ns * dn_stage;
   e = cudaFuncSetAttribute(k_tc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
   if (e != cudaSuccess) return e;
-  const int nsplit = tc_down_splits(L);
-  dim3 grid_dn(L->d / kTile + (L->d % kTile ? 1 : 0), nsplit);
-  k_tc_down<<<grid_dn, 128, dn_smem, s>>>(L->W_dT, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns,
+  const int ctiles = (L->d + cw * kTile - 1) / (cw * kTile);
+  int nsplit = L->num_sms / ctiles;
+  if (nsplit < 1) nsplit = 1;
+  dim3 grid_dn(ctiles, nsplit);
+  k_tc_down<<<grid_dn, 128, dn_smem, s>>>(L->W_dT, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns, cw,
                                          partial, L->status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
