@@ -74,7 +74,7 @@ struct LayerDev {
 struct StackParams {
   int n_layers, d, ffn, rank;
   int G, staged, lanes_l, pf_rows, pf_next;
-  int off_flag, off_list, off_lb, off_stage, stage_bytes;   // shared memory layout
+  int off_flag, off_list, off_lb, off_a, off_stage, stage_bytes, slice_pad;   // shared memory layout
   int soff_c, soff_b, soff_p1, soff_p2;                     // offsets inside a stage buffer
   const __half *x;       // [n_layers, B, d]
   float *y;              // [n_layers, B, d]

@@ -158,11 +158,11 @@ template <int CPT, int NB, bool REGLU>
 __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constant__ pi::StackParams p) {
   constexpr int NR = REGLU ? 2 : 1;                          // gated rows per neuron
   constexpr int LOADS = CPT == 1 ? 24 : 16;                  // 16-byte loads in flight per thread
-  constexpr int GW0 = LOADS / (CPT * (NR + 1));
-  constexpr int GW = GW0 > 0 ? GW0 : 1;                      // neurons per phase-E window
+  constexpr int GU0 = LOADS / (CPT * NR), GD0 = LOADS / CPT;
+  constexpr int GU = GU0 > 0 ? GU0 : 1;                      // neurons per up-pass window
+  constexpr int GD = GD0 > 0 ? GD0 : 1;                      // neurons per down-pass window
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float red_s[kWarps][NB][NR][GW];
-  __shared__ float a_s[NB][GW];
+  __shared__ float red_s[kWarps][NB][NR][GU];
   __shared__ float ared_s[kWarps][NB][8];
   __shared__ float4 fred_s[2][8];
   __shared__ int wtot_s[kWarps];
@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   unsigned char *flag_s = reinterpret_cast<unsigned char *>(smem) + p.off_flag;    // [slice]
   int *list_s = reinterpret_cast<int *>(smem + p.off_list);                        // [slice]
   float *lb_s = reinterpret_cast<float *>(smem + p.off_lb);                        // [slice] b of list
+  float *a_all = reinterpret_cast<float *>(smem + p.off_a);                         // [NB, slice] a of list
   // two stage buffers (layer l uses buffer l & 1), each [x | c_p slice | b slice | W_p1 rows | W_p2 slice]
   auto stage_buf = [&](int k) { return smem + p.off_stage + (size_t)k * p.stage_bytes; };
   const int s0a = s0 & ~3;                       // c / b slices start at this neuron
@@ -297,7 +298,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     for (int e = tid; e < NB * r; e += kThreads) h_s[e] = ldcg(p.h + e);
     __syncthreads();
     PHASE_STAMP(l, 9);
-    {
+    if (p.staged) {
+      // W_p2 slice in shared memory: one thread per row, vectors visited in
+      // a lane-rotated order so the 16-byte reads of a warp hit distinct banks
+      const int nvr = r >> 3;
+      for (int rl = tid; rl < n_rows; rl += kThreads) {
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(p2_s + (size_t)rl * r);
+        float a4[NB][4];
+#pragma unroll
+        for (int t = 0; t < NB; ++t)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) a4[t][q] = 0.f;
+        int vv = lane % nvr;
+        for (int v = 0; v < nvr; ++v) {
+          const uint4 wv = wrow[vv];
+          const __half2 *wh = reinterpret_cast<const __half2 *>(&wv);
+          const float2 w0 = __half22float2(wh[0]), w1 = __half22float2(wh[1]);
+          const float2 w2 = __half22float2(wh[2]), w3 = __half22float2(wh[3]);
+#pragma unroll
+          for (int t = 0; t < NB; ++t) {
+            const float4 *hp = reinterpret_cast<const float4 *>(h_s + t * r + vv * 8);
+            const float4 h0 = hp[0], h1 = hp[1];
+            a4[t][0] = fmaf(w0.x, h0.x, fmaf(w0.y, h0.y, a4[t][0]));
+            a4[t][1] = fmaf(w1.x, h0.z, fmaf(w1.y, h0.w, a4[t][1]));
+            a4[t][2] = fmaf(w2.x, h1.x, fmaf(w2.y, h1.y, a4[t][2]));
+            a4[t][3] = fmaf(w3.x, h1.z, fmaf(w3.y, h1.w, a4[t][3]));
+          }
+          vv = vv + 1 == nvr ? 0 : vv + 1;
+        }
+        bool on = false;
+#pragma unroll
+        for (int t = 0; t < NB; ++t)
+          on |= ((a4[t][0] + a4[t][1]) + (a4[t][2] + a4[t][3]) + c_s[s0 + rl - s0a]) > 0.f;
+        flag_s[rl] = on ? 1 : 0;
+      }
+    } else {
       const int GL = p.lanes_l;                 // lanes per predictor row (8, 16, 32)
       const int rows_per_warp = 32 / GL;
       const int sub = lane % GL;
@@ -421,7 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     PHASE_STAMP(l, 3);
     CTA_E_BEGIN(l);
 
-    // ---------------- E: up (+gate) and down rows of my active neurons
+    // ---------------- E: up (+gate) and down rows of my active neurons, in
+    // two passes: all up-row dot products first (a into shared memory), then
+    // all down rows.  The down rows were asked of L2 at the end of phase C,
+    // so they arrive while the up pass runs, and a CTA with many active
+    // neurons needs no extra round trip per extra window.
     float acc[NB][CPT][8];
 #pragma unroll
     for (int t = 0; t < NB; ++t)
@@ -429,19 +468,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       for (int c = 0; c < CPT; ++c)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[t][c][e] = 0.f;
-
-    for (int w0 = 0; w0 < lcount; w0 += GW) {
-      const int n_here = min(GW, lcount - w0);
-      if (w0 + GW > p.pf_rows)                  // rows past the early-prefetch budget
-        for (int j = max(w0, p.pf_rows) + tid; j < w0 + n_here; j += kThreads) {
-          const int i = list_s[j];
-          pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
-          if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
-          pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
-        }
-      uint4 wu[GW][NR][CPT], wd[GW][CPT];
+    if (lcount > p.pf_rows)                     // rows past the early-prefetch budget
+      for (int j = p.pf_rows + tid; j < lcount; j += kThreads) {
+        const int i = list_s[j];
+        pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
+        if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
+        pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+      }
+    for (int w0 = 0; w0 < lcount; w0 += GU) {
+      const int n_here = min(GU, lcount - w0);
+      uint4 wu[GU][NR][CPT];
 #pragma unroll
-      for (int n = 0; n < GW; ++n) {
+      for (int n = 0; n < GU; ++n) {
         const int i = n < n_here ? list_s[w0 + n] : -1;
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
@@ -452,26 +490,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           if (REGLU)
             wu[n][NR - 1][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_gate + (size_t)i * d) + v)
                                   : make_uint4(0, 0, 0, 0);
-          wd[n][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_dT + (size_t)i * d) + v)
-                        : make_uint4(0, 0, 0, 0);
         }
       }
 #pragma unroll
-      for (int n = 0; n < GW; ++n)
+      for (int n = 0; n < GU; ++n)
 #pragma unroll
         for (int q = 0; q < NR; ++q)
 #pragma unroll
           for (int t = 0; t < NB; ++t) {
-            float s = 0.f;
+            float sdot = 0.f;
 #pragma unroll
-            for (int c = 0; c < CPT; ++c) s = pidev::dot8(s, wu[n][q][c], xr[t][c]);
-            s = pidev::warp_sum(s);
-            if (lane == 0) red_s[wid][t][q][n] = s;
+            for (int c = 0; c < CPT; ++c) sdot = pidev::dot8(sdot, wu[n][q][c], xr[t][c]);
+            sdot = pidev::warp_sum(sdot);
+            if (lane == 0) red_s[wid][t][q][n] = sdot;
           }
       __syncthreads();
-      if (tid < NB * GW) {
-        const int t = tid / GW, n = tid % GW;
-        float a = 0.f;
+      if (tid < NB * GU) {
+        const int t = tid / GU, n = tid % GU;
         if (n < n_here) {
           const float bi = lb_s[w0 + n];
           float su = 0.f, sg = 0.f;
@@ -479,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
             su += red_s[q][t][0][n];
             if (REGLU) sg += red_s[q][t][NR - 1][n];
           }
+          float a;
           if (REGLU) {
             const float gz = sg + bi;
             a = (gz > 0.f ? gz : 0.f) * su;
@@ -486,19 +522,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
             const float z = su + bi;
             a = z > 0.f ? z : 0.f;
           }
+          a_all[t * p.slice_pad + w0 + n] = a;
         }
-        a_s[t][n] = a;
       }
-      __syncthreads();
+      __syncthreads();   // red_s is rewritten by the next window
+    }
+    for (int w0 = 0; w0 < lcount; w0 += GD) {
+      const int n_here = min(GD, lcount - w0);
+      uint4 wd[GD][CPT];
 #pragma unroll
-      for (int n = 0; n < GW; ++n)
+      for (int n = 0; n < GD; ++n) {
+        const int i = n < n_here ? list_s[w0 + n] : -1;
 #pragma unroll
-        for (int t = 0; t < NB; ++t) {
-          const float an = a_s[t][n];
-#pragma unroll
-          for (int c = 0; c < CPT; ++c) pidev::axpy8(acc[t][c], an, wd[n][c]);
+        for (int c = 0; c < CPT; ++c) {
+          const int v = tid + c * kThreads;
+          wd[n][c] = (i >= 0 && v < nv)
+                         ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_dT + (size_t)i * d) + v)
+                         : make_uint4(0, 0, 0, 0);
         }
-      __syncthreads();   // red_s / a_s are rewritten by the next window
+      }
+#pragma unroll
+      for (int n = 0; n < GD; ++n) {
+        if (n < n_here) {
+#pragma unroll
+          for (int t = 0; t < NB; ++t) {
+            const float an = a_all[t * p.slice_pad + w0 + n];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) pidev::axpy8(acc[t][c], an, wd[n][c]);
+          }
+        }
+      }
     }
     PHASE_STAMP(l, 4);
     CTA_E_END(l, lcount);
@@ -626,9 +679,10 @@ cudaError_t dispatch_step(const pi::StackParams &p, size_t smem, cudaStream_t s)
 constexpr size_t kSmemBudget = 200 * 1024;   // dynamic shared memory the step may use
 
 size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
+size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
 struct SmemPlan {
-  size_t off_flag, off_list, off_lb, off_stage;          // absolute offsets
+  size_t off_flag, off_list, off_lb, off_a, off_stage;   // absolute offsets
   size_t soff_c, soff_b, soff_p1, soff_p2;              // offsets inside a stage buffer
   size_t stage_small, stage_full;                        // buffer size without / with predictor
   size_t base_end;
@@ -643,6 +697,7 @@ SmemPlan smem_plan(const pi_layer *L, int B) {
   s.off_flag = off;  off = align128(off + slice);
   s.off_list = off;  off = align128(off + sizeof(int) * slice);
   s.off_lb = off;    off = align128(off + sizeof(float) * slice);
+  s.off_a = off;     off = align128(off + sizeof(float) * (size_t)B * align16(slice));
   s.off_stage = off;
   s.base_end = off;
   size_t so = align128(2 * (size_t)B * L->d);                     // x
@@ -687,6 +742,8 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   p.off_flag = (int)sp.off_flag;
   p.off_list = (int)sp.off_list;
   p.off_lb = (int)sp.off_lb;
+  p.off_a = (int)sp.off_a;
+  p.slice_pad = (int)align16((size_t)step_slice(L0));
   p.off_stage = (int)sp.off_stage;
   p.stage_bytes = (int)(p.staged ? sp.stage_full : sp.stage_small);
   p.soff_c = (int)sp.soff_c;
