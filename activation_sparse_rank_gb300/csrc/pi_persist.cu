@@ -31,6 +31,10 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+// The last warp issues the asynchronous copies and prefetches (TMA staging,
+// L2 prefetch): those instructions can stall their issuing thread, so they
+// go to a warp that has no other work on the critical path.
+constexpr int kIssuer = kThreads - 32;
 constexpr unsigned kSpinLimit = 1u << 22;   // polls before a wait gives up (seconds)
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (tid == 0) stage(0);
+  if (tid == kIssuer) stage(0);
 
   for (int l = 0; l < p.n_layers; ++l) {
     const pi::LayerDev &Ld = p.layers[l];
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
 
     const uint32_t mbar = mbar0 + 8u * (uint32_t)(l & 1);
     // the next layer's inputs go to the other buffer, free since the last barrier
-    if (tid == 0 && l + 1 < p.n_layers) stage(l + 1);
+    if (tid == kIssuer && l + 1 < p.n_layers) stage(l + 1);
     const int n_hot = min(Ld.hot_per_slice, n_rows);
     if (!mbar_wait(mbar, (uint32_t)((l >> 1) & 1))) {
       if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
@@ -263,11 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q)
+        if (cta + (q0 + q) * G < r)              // uniform over the CTA
 #pragma unroll
-        for (int t = 0; t < NB; ++t) {
-          const float s = pidev::warp_sum(hs[q][t]);
-          if (lane == 0) ared_s[wid][t][q] = s;
-        }
+          for (int t = 0; t < NB; ++t) {
+            const float s = pidev::warp_sum(hs[q][t]);
+            if (lane == 0) ared_s[wid][t][q] = s;
+          }
       __syncthreads();
       if (tid < 8 * NB) {
         const int q = tid / NB, t = tid % NB;
@@ -289,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     // fire on most tokens: start their rows towards L2 now, while HBM would
     // otherwise idle through the logits.  (Issued after barrier 1: a burst
     // before it slowed the barrier itself.)
-    if (tid >= 32 && tid < 32 + n_hot) {
-      const int i = s0 + tid - 32;
+    if (tid >= kIssuer && tid < kIssuer + n_hot) {
+      const int i = s0 + tid - kIssuer;
       pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
       if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
       pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
@@ -431,13 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       PHASE_STAMP(l, 11);
       // ask L2 for all my active rows now (bounded by the prefetch budget)
       const int npf = min(lcount, p.pf_rows);
-      for (int j = tid; j < npf; j += kThreads) {
-        const int i = list_s[j];
-        if (i - s0 < n_hot) continue;          // requested at layer start
-        pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
-        if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
-        pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
-      }
+      if (tid >= kIssuer)
+        for (int j = tid - kIssuer; j < npf; j += 32) {
+          const int i = list_s[j];
+          if (i - s0 < n_hot) continue;        // requested after the first barrier
+          pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
+          if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
+          pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+        }
       for (int j = tid; j < lcount; j += kThreads) lb_s[j] = b_s[list_s[j] - s0a];
       if (p.mask_out)
         for (int i = tid; i < n_rows; i += kThreads) p.mask_out[(size_t)l * ffn + s0 + i] = flag_s[i];
