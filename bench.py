@@ -258,9 +258,12 @@ def max_over_ranks(value: float, device=None) -> float:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the persistent step kernel's sources: the stored DRAM counters
+    hold only while it matches."""
     h = hashlib.sha256()
-    for p in sorted((ROOT / "activation_sparse_rank_gb300" / "csrc").glob("*")):
-        h.update(p.read_bytes())
+    csrc = ROOT / "activation_sparse_rank_gb300" / "csrc"
+    for name in ("pi_internal.cuh", "pi_persist.cu"):
+        h.update((csrc / name).read_bytes())
     return h.hexdigest()[:16]
 
 
