@@ -57,11 +57,14 @@ struct WsLayout {
   size_t bar = 0;      // uint32                grid-barrier counter
   size_t abuf = 0;     // fp16 [2*Bp, ffn_pad]  activations (hi; lo) of the tensor-core path
   size_t hbuf = 0;     // fp16 [2*Bp, rank_pad] predictor hidden layer (hi; lo), tensor-core path
+  size_t hpart = 0;    // float [splits, Bp, rank_pad] its split-K partial sums
   size_t total = 0;
 };
 
 // Layers per persistent launch (longer stacks are split into several launches).
 constexpr int kMaxStack = 64;
+// Upper bound on the K splits of the tensor-core predictor's hidden layer.
+constexpr int kMaxHiddenSplits = 32;
 
 // Device pointers of one layer, as the persistent kernel sees them.
 struct LayerDev {
@@ -139,9 +142,11 @@ int tc_bpad(int B);
 int tc_ffn_pad(const pi_layer *L);
 bool tc_predict_supported(const pi_layer *L, int B);
 int tc_rank_pad(const pi_layer *L);
-// h (fp16 pair, in hbuf [2Bp, rank_pad]) and the batch-union mask [ffn] on the tensor cores
+// h (fp16 pair, in hbuf [2Bp, rank_pad]) and the batch-union mask [ffn] on the
+// tensor cores; hpart: fp32 scratch [tc_hidden_splits, Bp, rank_pad].
 cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
-                           cudaStream_t s);
+                           float *hpart, cudaStream_t s);
+int tc_hidden_splits(const pi_layer *L);
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,
                               char *ws, cudaStream_t s);

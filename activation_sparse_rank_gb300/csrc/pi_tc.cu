@@ -29,6 +29,8 @@
 // waits (bounded) for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "pi_internal.cuh"
 
 namespace {
@@ -139,22 +141,28 @@ __device__ __forceinline__ int tmem_cols_for(int n) {
 // three epilogues:
 //   kAct     a = ReLU(D + bias) (ReGLU: ReLU(D_gate + bias) * D_up), written
 //            as the fp16 pair (hi; lo) into out [2Bp, ld] (the sparse FFN up)
-//   kHidden  h = ReLU(D), written as the pair into out (predictor layer 1)
 //   kLogits  l = D_hi + D_lo + bias over the pair columns of Bop; mask[row] =
 //            1 if l > 0 for some token of the batch (predictor layer 2)
-constexpr int kAct = 0, kHidden = 1, kLogits = 2;
+//   kHiddenPart  the predictor's layer 1 split over K: CTA (tile, blockIdx.y)
+//            contracts K elements [blockIdx.y * klen, +klen) and writes D in
+//            fp32 to fout [split, Bp, ld]; k_hidden_finish adds the splits
+//            in order.  (The layer has only r / 128 row tiles, too few CTAs
+//            to stream W_p1 at speed.)
+constexpr int kAct = 0, kHiddenPart = 1, kLogits = 2;
 
 template <int MODE, bool REGLU>
 __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ Wg,   // rows (gated rows for kAct)
                                                     const __half *__restrict__ Wu,   // up rows (ReGLU)
                                                     const __grid_constant__ CUtensorMap tm_x,   // B operand
                                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
-                                                    int count_const, const float *__restrict__ bias, int d, int ffn,
-                                                    int B, int Bp, int nstage, int kw, __half *__restrict__ abuf,
-                                                    int abuf_ld, uint8_t *__restrict__ mask_out, unsigned int *status) {
-  // d: row length and contraction length K; ffn: number of rows of W.  A
-  // pipeline stage holds kw consecutive 64-element K slabs, so every gathered
-  // row contributes kw * 128 contiguous bytes per stage.
+                                                    int count_const, const float *__restrict__ bias, int d, int klen,
+                                                    int ffn, int B, int Bp, int nstage, int kw,
+                                                    __half *__restrict__ abuf, float *__restrict__ fout, int abuf_ld,
+                                                    uint8_t *__restrict__ mask_out, unsigned int *status) {
+  // d: row length of W; this CTA contracts K elements [koff, koff + klen);
+  // ffn: number of rows of W.  A pipeline stage holds kw consecutive
+  // 64-element K slabs, so every gathered row contributes kw * 128
+  // contiguous bytes per stage.
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   constexpr int NA = REGLU ? 2 : 1;
@@ -194,7 +202,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
     count = count < 0 ? 0 : ffn;
   }
   const int ntiles = (count + kTile - 1) / kTile;
-  const int KT = d / (kSlab * kw);
+  const int koff = (int)blockIdx.y * klen;
+  const int KT = klen / (kSlab * kw);
   const uint32_t idesc = idesc_f16(Nmma, kTile, false);
   uint32_t gslab = 0;          // slabs issued by this CTA so far (pipeline position)
   uint32_t done_phase = 0;
@@ -223,8 +232,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
       for (int i = 0; i < 8; ++i) {
         const int q = (tid >> 3) + 16 * i;
         const int rid = rows_s[q] >= 0 ? rows_s[q] : 0;
-        gsrc[i] = Wg + (size_t)rid * d + cch * 8;
-        usrc[i] = REGLU ? Wu + (size_t)rid * d + cch * 8 : nullptr;
+        gsrc[i] = Wg + (size_t)rid * d + koff + cch * 8;
+        usrc[i] = REGLU ? Wu + (size_t)rid * d + koff + cch * 8 : nullptr;
       }
       auto issue = [&](int kt, uint32_t g) {
         const int s = (int)(g % (uint32_t)nstage);
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
         if (tid == 0) {
           mb_expect(bar, kw * slabX);
           for (int j = 0; j < kw; ++j)
-            tma_tile2d(su32(st + NA * kw * slabA + j * subX), &tm_x, (kt * kw + j) * kSlab, 0, bar);
+            tma_tile2d(su32(st + NA * kw * slabA + j * subX), &tm_x, koff + (kt * kw + j) * kSlab, 0, bar);
         }
       };
       const int pre = min(nstage - 1, KT);
@@ -303,6 +312,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
           if (c0 + j < B) on |= (hi8[j] + lo8[j] + bi) > 0.f;
       }
       if (i >= 0) mask_out[i] = on ? 1 : 0;
+    } else if (MODE == kHiddenPart) {
+      float *dst = fout + (size_t)blockIdx.y * Bp * abuf_ld + kq;
+      for (int c0 = 0; c0 < Bp; c0 += 8) {
+        float g8[8];
+        tmem_ld8(trow + (uint32_t)c0, g8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[(size_t)(c0 + j) * abuf_ld] = (i >= 0 && c0 + j < B) ? g8[j] : 0.f;
+      }
     } else {
       for (int c0 = 0; c0 < Bp; c0 += 8) {
         float g8[8], u8[8];
@@ -523,18 +540,37 @@ bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// h = ReLU(sum of the K splits, in split order), written as the fp16 pair
+// (hi rows 0..Bp-1, lo rows Bp..2Bp-1) of the logits kernel's B operand.
+__global__ void k_hidden_finish(const float *__restrict__ part, int nsplit, int B, int Bp, int rank, int rpad,
+                                __half *__restrict__ hbuf) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = Bp * rpad;
+  if (e >= n) return;
+  const int b = e / rpad, row = e % rpad;
+  float acc = 0.f;
+  for (int k = 0; k < nsplit; ++k) acc += part[(size_t)k * n + e];
+  const float h = (b < B && row < rank && acc > 0.f) ? acc : 0.f;
+  const __half hi = __float2half_rn(h);
+  hbuf[e] = hi;
+  hbuf[(size_t)n + e] = __float2half_rn(h - __half2float(hi));
+}
+
 constexpr size_t kTcSmemBudget = 200 * 1024;
 
 template <int MODE, bool REGLU>
 cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, const CUtensorMap &tm_x,
                         const int32_t *idx, const int32_t *count, int count_const, const float *bias, int K,
-                        int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, cudaStream_t s) {
+                        int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, cudaStream_t s,
+                        int ksplit = 1, float *fout = nullptr) {
+  // K: row length; each of the ksplit CTAs of a row tile contracts K / ksplit
+  const int klen = K / ksplit;
   const int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const size_t sub = NA * (size_t)kTile * 128 + (((size_t)Nmma * 128 + 1023) & ~(size_t)1023);
   // widest stage (kw consecutive slabs per row) that divides K and keeps >= 2 stages
   int kw = 4;
-  while (kw > 1 && ((K / kSlab) % kw != 0 || (kTcSmemBudget - 1024) / (kw * sub) < 2)) kw >>= 1;
+  while (kw > 1 && ((klen / kSlab) % kw != 0 || (kTcSmemBudget - 1024) / (kw * sub) < 2)) kw >>= 1;
   const size_t stage = kw * sub;
   int ns = (int)((kTcSmemBudget - 1024) / stage);
   if (ns > 8) ns = 8;
@@ -545,8 +581,8 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   if (e != cudaSuccess) return e;
   int grid = (nrows + kTile - 1) / kTile;
   if (grid > L->num_sms) grid = L->num_sms;
-  kern<<<grid, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, kw, out, out_ld,
-                               mask, L->status);
+  kern<<<dim3(grid, ksplit), 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, klen, nrows, B, Bp,
+                                             ns, kw, out, fout, out_ld, mask, L->status);
   return cudaGetLastError();
 }
 
@@ -568,17 +604,30 @@ bool tc_predict_supported(const pi_layer *L, int B) {
 
 int tc_rank_pad(const pi_layer *L) { return (L->rank + kTile - 1) / kTile * kTile; }
 
+int tc_hidden_splits(const pi_layer *L) {
+  const int tiles = tc_rank_pad(L) / kTile, slabs = L->d / kSlab;
+  int k = std::min(kMaxHiddenSplits, std::max(1, L->num_sms / tiles));
+  while (k > 1 && slabs % k != 0) --k;
+  return k;
+}
+
 cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
-                           cudaStream_t s) {
+                           float *hpart, cudaStream_t s) {
   const int Bp = tc_bpad(B);
   const int rpad = tc_rank_pad(L);
   CUtensorMap tm_x, tm_h;
   if (!encode_2d(&tm_x, x, L->d, B, (uint64_t)L->d * 2, kSlab, Bp) ||
       !encode_2d(&tm_h, hbuf, rpad, 2 * Bp, (uint64_t)rpad * 2, kSlab, 2 * Bp))
     return cudaErrorInvalidValue;
-  // h = ReLU(W_p1 x) as an fp16 pair, then l = W_p2 h + c_p -> union mask
-  cudaError_t e = launch_rows<kHidden, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr, L->d,
-                                              L->rank, B, Bp, hbuf, rpad, nullptr, s);
+  // h = ReLU(W_p1 x) as an fp16 pair (K split over CTAs, splits added in
+  // order), then l = W_p2 h + c_p -> union mask
+  const int ks = tc_hidden_splits(L);
+  cudaError_t e = launch_rows<kHiddenPart, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr,
+                                                  L->d, L->rank, B, Bp, nullptr, rpad, nullptr, s, ks, hpart);
+  if (e != cudaSuccess) return e;
+  const int n = Bp * rpad;
+  k_hidden_finish<<<(n + 255) / 256, 256, 0, s>>>(hpart, ks, B, Bp, L->rank, rpad, hbuf);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->ffn, B,
                                      Bp, nullptr, 0, mask_union, s);
