@@ -180,7 +180,7 @@ WsLayout ws_layout(const pi_layer *L, int B) {
   w.bar = off;     off += align_up(sizeof(unsigned));
   w.abuf = off;    off += align_up(2 * sizeof(__half) * (size_t)tc_bpad(B) * tc_ffn_pad(L));
   w.hbuf = off;    off += align_up(2 * sizeof(__half) * (size_t)tc_bpad(B) * tc_rank_pad(L));
-  w.hpart = off;   off += B >= 3 ? align_up(sizeof(float) * (size_t)kMaxHiddenSplits * tc_bpad(B) * tc_rank_pad(L)) : 0;
+  w.tcpart = off;  off += B >= 3 ? align_up(tc_piece_bytes(L, B)) : 0;
   w.total = off;
   return w;
 }
@@ -457,7 +457,7 @@ pi_status pi_layer_forward(pi_layer *L, const uint16_t *x, int32_t B, int32_t *i
   uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
   if (pi::tc_predict_supported(L, B))
     PI_TRY_CUDA(pi::run_predict_tc(L, xh, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
-                                    reinterpret_cast<float *>(wsb + w.hpart), s));
+                                    reinterpret_cast<float *>(wsb + w.tcpart), s));
   else
     PI_TRY_CUDA(pi::run_predict(L, xh, B, mask, nullptr, reinterpret_cast<float *>(wsb + w.h), s, true));
   PI_TRY_CUDA(pi::run_compact(L, mask, 1, idx, count, s));
@@ -504,7 +504,7 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
     uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
     if (pi::tc_predict_supported(Ll, B))
       PI_TRY_CUDA(pi::run_predict_tc(Ll, xh + l * xs, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
-                                      reinterpret_cast<float *>(wsb + w.hpart), s));
+                                      reinterpret_cast<float *>(wsb + w.tcpart), s));
     else
       PI_TRY_CUDA(pi::run_predict(Ll, xh + l * xs, B, mask, nullptr, reinterpret_cast<float *>(wsb + w.h), s, true));
     PI_TRY_CUDA(pi::run_compact(Ll, mask, 1, idx + (size_t)l * L->ffn, count + l, s));

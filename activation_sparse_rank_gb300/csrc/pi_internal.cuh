@@ -57,14 +57,13 @@ struct WsLayout {
   size_t bar = 0;      // uint32                grid-barrier counter
   size_t abuf = 0;     // fp16 [2*Bp, ffn_pad]  activations (hi; lo) of the tensor-core path
   size_t hbuf = 0;     // fp16 [2*Bp, rank_pad] predictor hidden layer (hi; lo), tensor-core path
-  size_t hpart = 0;    // float [splits, Bp, rank_pad] its split-K partial sums
+  size_t tcpart = 0;   // float [2 G, 2 Bp, 128] tensor-core tiles split between CTAs
   size_t total = 0;
 };
 
 // Layers per persistent launch (longer stacks are split into several launches).
 constexpr int kMaxStack = 64;
-// Upper bound on the K splits of the tensor-core predictor's hidden layer.
-constexpr int kMaxHiddenSplits = 32;
+
 
 // Device pointers of one layer, as the persistent kernel sees them.
 struct LayerDev {
@@ -143,10 +142,10 @@ int tc_ffn_pad(const pi_layer *L);
 bool tc_predict_supported(const pi_layer *L, int B);
 int tc_rank_pad(const pi_layer *L);
 // h (fp16 pair, in hbuf [2Bp, rank_pad]) and the batch-union mask [ffn] on the
-// tensor cores; hpart: fp32 scratch [tc_hidden_splits, Bp, rank_pad].
+// tensor cores; piece: fp32 scratch of tc_piece_bytes for tiles split between CTAs.
 cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
-                           float *hpart, cudaStream_t s);
-int tc_hidden_splits(const pi_layer *L);
+                           float *piece, cudaStream_t s);
+size_t tc_piece_bytes(const pi_layer *L, int B);
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,
                               char *ws, cudaStream_t s);

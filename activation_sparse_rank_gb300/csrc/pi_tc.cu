@@ -141,32 +141,101 @@ __device__ __forceinline__ int tmem_cols_for(int n) {
 // three epilogues:
 //   kAct     a = ReLU(D + bias) (ReGLU: ReLU(D_gate + bias) * D_up), written
 //            as the fp16 pair (hi; lo) into out [2Bp, ld] (the sparse FFN up)
+//   kHidden  h = ReLU(D), written as the pair into out (predictor layer 1)
 //   kLogits  l = D_hi + D_lo + bias over the pair columns of Bop; mask[row] =
 //            1 if l > 0 for some token of the batch (predictor layer 2)
-//   kHiddenPart  the predictor's layer 1 split over K: CTA (tile, blockIdx.y)
-//            contracts K elements [blockIdx.y * klen, +klen) and writes D in
-//            fp32 to fout [split, Bp, ld]; k_hidden_finish adds the splits
-//            in order.  (The layer has only r / 128 row tiles, too few CTAs
-//            to stream W_p1 at speed.)
-constexpr int kAct = 0, kHiddenPart = 1, kLogits = 2;
+//
+// Work is split stream-K style: the (tile, K stage) iterations of all row
+// tiles are laid end to end and CTA c takes the contiguous range
+// [c*I/G, (c+1)*I/G), so every CTA streams the same number of bytes whatever
+// the tile count (a union of 171 tiles on 152 SMs, or the predictor's r/128
+// tiles, no longer leaves SMs idle).  A tile covered by one CTA gets its
+// epilogue at once; a tile split between CTAs leaves one fp32 piece per CTA
+// (slot 2c for a CTA's first piece, 2c+1 for its last) and k_tc_fixup adds
+// the pieces in CTA order (deterministic) and applies the epilogue.
+constexpr int kAct = 0, kHidden = 1, kLogits = 2;
+
+__device__ __forceinline__ long long range_start(int c, long long I, int G) { return (long long)c * I / G; }
+
+// At most kCtasPerTile CTAs per row tile take part (a small list leaves the
+// rest of the grid idle rather than cutting tiles into slivers); a tile then
+// meets at most 2 * kCtasPerTile + 2 CTA ranges, within kMaxPieces.
+constexpr int kCtasPerTile = 8;
+constexpr int kMaxPieces = 32;
+
+__device__ __forceinline__ int active_ctas(int grid, int ntiles) {
+  const long long g = (long long)ntiles * kCtasPerTile;
+  return (int)(g < grid ? (g > 0 ? g : 1) : grid);
+}
+
+// Row of a tile: index into W (or -1 past the end of the list, -2 when the
+// list holds an out-of-range index, which is flagged).
+__device__ __forceinline__ int tile_row(const int32_t *idx, int k, int count, int ffn, unsigned *status) {
+  if (k >= count) return -1;
+  const int i = idx ? idx[k] : k;
+  if (i < 0 || i >= ffn) {
+    atomicOr(status, PI_STATUS_BAD_INDEX);
+    return -2;
+  }
+  return i;
+}
+
+// Epilogue of one tile row (the calling thread's row q, W row i, output
+// column kq).  fetch8(c, v) yields D columns c .. c+7 of the row; for kAct
+// and kHidden only token columns [c_begin, c_end) are produced.
+template <int MODE, bool REGLU, typename F>
+__device__ __forceinline__ void row_epilogue(F fetch8, int c_begin, int c_end, int i, int kq, float bi, int B,
+                                             int Bp, int Nmma, __half *abuf, int abuf_ld, uint8_t *mask_out) {
+  if (MODE == kLogits) {
+    bool on = false;
+    for (int c0 = 0; c0 < Bp; c0 += 8) {
+      float hi8[8], lo8[8];
+      fetch8(c0, hi8);
+      fetch8(Bp + c0, lo8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < B) on |= (hi8[j] + lo8[j] + bi) > 0.f;
+    }
+    if (i >= 0) mask_out[i] = on ? 1 : 0;
+  } else {
+    for (int c0 = c_begin; c0 < c_end; c0 += 8) {
+      float g8[8], u8[8];
+      fetch8(c0, g8);
+      if (REGLU) fetch8(Nmma + c0, u8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int b = c0 + j;
+        float a = 0.f;
+        if (i >= 0 && b < B) {
+          const float z = g8[j] + bi;
+          a = REGLU ? (z > 0.f ? z : 0.f) * u8[j] : (z > 0.f ? z : 0.f);
+        }
+        const __half hi = __float2half_rn(a);
+        const __half lo = __float2half_rn(a - __half2float(hi));
+        abuf[(size_t)b * abuf_ld + kq] = hi;
+        abuf[(size_t)(Bp + b) * abuf_ld + kq] = lo;
+      }
+    }
+  }
+}
 
 template <int MODE, bool REGLU>
 __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ Wg,   // rows (gated rows for kAct)
                                                     const __half *__restrict__ Wu,   // up rows (ReGLU)
                                                     const __grid_constant__ CUtensorMap tm_x,   // B operand
                                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
-                                                    int count_const, const float *__restrict__ bias, int d, int klen,
-                                                    int ffn, int B, int Bp, int nstage, int kw,
-                                                    __half *__restrict__ abuf, float *__restrict__ fout, int abuf_ld,
+                                                    int count_const, const float *__restrict__ bias, int d, int ffn,
+                                                    int B, int Bp, int nstage, int kw, __half *__restrict__ abuf,
+                                                    int abuf_ld, float *__restrict__ piece,
                                                     uint8_t *__restrict__ mask_out, unsigned int *status) {
-  // d: row length of W; this CTA contracts K elements [koff, koff + klen);
-  // ffn: number of rows of W.  A pipeline stage holds kw consecutive
-  // 64-element K slabs, so every gathered row contributes kw * 128
-  // contiguous bytes per stage.
+  // d: row length of W and contraction length K; ffn: number of rows of W.
+  // A pipeline stage holds kw consecutive 64-element K slabs, so every
+  // gathered row contributes kw * 128 contiguous bytes per stage.
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   constexpr int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
+  const int ncolD = NA * Nmma;                          // accumulator columns
   const uint32_t slabA = kTile * 128;                   // one gathered operand slab
   const uint32_t slabX = (uint32_t)Nmma * 128;
   const uint32_t subX = (slabX + 1023) & ~1023u;
@@ -177,7 +246,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
   __shared__ int fail_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ncols = tmem_cols_for(NA * Nmma);
+  const int ncols = tmem_cols_for(ncolD);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -202,23 +271,23 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
     count = count < 0 ? 0 : ffn;
   }
   const int ntiles = (count + kTile - 1) / kTile;
-  const int koff = (int)blockIdx.y * klen;
-  const int KT = klen / (kSlab * kw);
+  const int KT = d / (kSlab * kw);                      // stages per tile
+  const long long I = (long long)ntiles * KT;
+  const int G = active_ctas(gridDim.x, ntiles), cta = blockIdx.x;
+  const long long rs = cta < G ? range_start(cta, I, G) : 0, re = cta < G ? range_start(cta + 1, I, G) : 0;
   const uint32_t idesc = idesc_f16(Nmma, kTile, false);
-  uint32_t gslab = 0;          // slabs issued by this CTA so far (pipeline position)
+  uint32_t gslab = 0;          // stages issued by this CTA so far (pipeline position)
   uint32_t done_phase = 0;
 
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+  for (long long s0 = rs; s0 < re;) {
+    const int tile = (int)(s0 / KT);
+    const int kb = (int)(s0 % KT);
+    const int n = (int)min((long long)(KT - kb), re - s0);   // stages of this piece
+    const bool whole = (n == KT);
+    const int slot = 2 * cta + (s0 == rs ? 0 : 1);
+    s0 += n;
     const int k0 = tile * kTile;
-    {
-      const int k = k0 + tid;
-      int i = k < count ? (idx ? idx[k] : k) : -1;
-      if (k < count && (i < 0 || i >= ffn)) {
-        atomicOr(status, PI_STATUS_BAD_INDEX);
-        i = -2;
-      }
-      rows_s[tid] = i;
-    }
+    rows_s[tid] = tile_row(idx, k0 + tid, count, ffn, status);
     __syncthreads();
     {
       // Every thread copies 8 of the 1024 16-byte chunks of each gathered
@@ -232,8 +301,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
       for (int i = 0; i < 8; ++i) {
         const int q = (tid >> 3) + 16 * i;
         const int rid = rows_s[q] >= 0 ? rows_s[q] : 0;
-        gsrc[i] = Wg + (size_t)rid * d + koff + cch * 8;
-        usrc[i] = REGLU ? Wu + (size_t)rid * d + koff + cch * 8 : nullptr;
+        gsrc[i] = Wg + (size_t)rid * d + cch * 8;
+        usrc[i] = REGLU ? Wu + (size_t)rid * d + cch * 8 : nullptr;
       }
       auto issue = [&](int kt, uint32_t g) {
         const int s = (int)(g % (uint32_t)nstage);
@@ -254,15 +323,15 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
         if (tid == 0) {
           mb_expect(bar, kw * slabX);
           for (int j = 0; j < kw; ++j)
-            tma_tile2d(su32(st + NA * kw * slabA + j * subX), &tm_x, koff + (kt * kw + j) * kSlab, 0, bar);
+            tma_tile2d(su32(st + NA * kw * slabA + j * subX), &tm_x, (kt * kw + j) * kSlab, 0, bar);
         }
       };
-      const int pre = min(nstage - 1, KT);
-      for (int kt = 0; kt < pre; ++kt) issue(kt, gslab + kt);
-      for (int kt = 0; kt < KT; ++kt) {
+      const int pre = min(nstage - 1, n);
+      for (int it = 0; it < pre; ++it) issue(kb + it, gslab + it);
+      for (int it = 0; it < n; ++it) {
         if (fail_s) break;
-        const uint32_t g = gslab + kt;
-        if (kt + nstage - 1 < KT) issue(kt + nstage - 1, g + nstage - 1);
+        const uint32_t g = gslab + it;
+        if (it + nstage - 1 < n) issue(kb + it + nstage - 1, g + nstage - 1);
         if (tid == 0) {
           const int s = (int)(g % (uint32_t)nstage);
           if (!mb_wait(su32(&full_s[s]), (g / nstage) & 1)) {
@@ -277,7 +346,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
-                const uint32_t acc = (kt | j | kk) ? 1u : 0u;
+                const uint32_t acc = (it | j | kk) ? 1u : 0u;
                 mma_f16(tmem, sdesc(aa + kk * 32, 16, 1024), bd, idesc, acc);
                 if (REGLU)
                   mma_f16(tmem + (uint32_t)Nmma, sdesc(aa + kw * slabA + kk * 32, 16, 1024), bd, idesc, acc);
@@ -287,7 +356,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
           }
         }
       }
-      gslab += KT;
+      gslab += n;
       if (tid == 0) mma_commit(su32(&done_s));
     }
     __syncthreads();
@@ -297,47 +366,19 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
     asm volatile("tcgen05.fence::after_thread_sync;");
     // epilogue: TMEM lane = tile row = warp*32 + lane
     const int q = warp * 32 + lane;
-    const int i = rows_s[q];
-    const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
-    const int kq = k0 + q;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    if (MODE == kLogits) {
-      bool on = false;
-      for (int c0 = 0; c0 < Bp; c0 += 8) {
-        float hi8[8], lo8[8];
-        tmem_ld8(trow + (uint32_t)c0, hi8);
-        tmem_ld8(trow + (uint32_t)(Bp + c0), lo8);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (c0 + j < B) on |= (hi8[j] + lo8[j] + bi) > 0.f;
-      }
-      if (i >= 0) mask_out[i] = on ? 1 : 0;
-    } else if (MODE == kHiddenPart) {
-      float *dst = fout + (size_t)blockIdx.y * Bp * abuf_ld + kq;
-      for (int c0 = 0; c0 < Bp; c0 += 8) {
-        float g8[8];
-        tmem_ld8(trow + (uint32_t)c0, g8);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dst[(size_t)(c0 + j) * abuf_ld] = (i >= 0 && c0 + j < B) ? g8[j] : 0.f;
-      }
+    if (whole) {
+      const int i = rows_s[q];
+      const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
+      row_epilogue<MODE, REGLU>([&](int c, float *v) { tmem_ld8(trow + (uint32_t)c, v); }, 0, Bp, i, k0 + q, bi, B,
+                                Bp, Nmma, abuf, abuf_ld, mask_out);
     } else {
-      for (int c0 = 0; c0 < Bp; c0 += 8) {
-        float g8[8], u8[8];
-        tmem_ld8(trow + (uint32_t)c0, g8);
-        if (REGLU) tmem_ld8(trow + (uint32_t)(Bp + c0), u8);
+      float *dst = piece + (size_t)slot * ncolD * kTile + q;
+      for (int c0 = 0; c0 < ncolD; c0 += 8) {
+        float v[8];
+        tmem_ld8(trow + (uint32_t)c0, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int b = c0 + j;
-          float a = 0.f;
-          if (i >= 0 && b < B) {
-            const float z = g8[j] + bi;
-            a = REGLU ? (z > 0.f ? z : 0.f) * u8[j] : (z > 0.f ? z : 0.f);
-          }
-          const __half hi = __float2half_rn(a);
-          const __half lo = __float2half_rn(a - __half2float(hi));
-          abuf[(size_t)b * abuf_ld + kq] = hi;
-          abuf[(size_t)(Bp + b) * abuf_ld + kq] = lo;
-        }
+        for (int j = 0; j < 8; ++j) dst[(size_t)(c0 + j) * kTile] = v[j];
       }
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
@@ -350,6 +391,77 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
+}
+
+// Tiles that k_tc_rows split between CTAs: block c finishes the tile whose
+// last stage lies in CTA c's range when that tile started in an earlier CTA's
+// range.  It adds the tile's pieces in CTA order and applies the epilogue to
+// token columns [8 * blockIdx.y, +8) (kLogits: all columns, one y block).
+template <int MODE, bool REGLU>
+__global__ void __launch_bounds__(128) k_tc_fixup(const float *__restrict__ piece, const int32_t *__restrict__ idx,
+                                                  const int32_t *__restrict__ count_p, int count_const,
+                                                  const float *__restrict__ bias, int ffn, int B, int Bp, int KT, int grid,
+                                                  __half *__restrict__ abuf, int abuf_ld,
+                                                  uint8_t *__restrict__ mask_out, unsigned int *status) {
+  constexpr int NA = REGLU ? 2 : 1;
+  const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
+  const int ncolD = NA * Nmma;
+  int count = count_p ? *count_p : count_const;
+  if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;    // flagged by k_tc_rows
+  const int ntiles = (count + kTile - 1) / kTile;
+  const long long I = (long long)ntiles * KT;
+  const int G = active_ctas(grid, ntiles), c = blockIdx.x;
+  if (c >= G) return;
+  const long long rs = range_start(c, I, G), re = range_start(c + 1, I, G);
+  if (rs >= re || rs % KT == 0) return;          // c's range starts a tile: it completes no split tile
+  const int tile = (int)(rs / KT);
+  const long long t0 = (long long)tile * KT, t1 = t0 + KT;
+  if (re < t1) return;                           // the tile goes on in a later CTA
+  __shared__ int slots_s[kMaxPieces];
+  __shared__ int nslot_s;
+  if (threadIdx.x == 0) {          // the tile's pieces, in CTA order
+    int cf = c;
+    while (cf > 0 && range_start(cf, I, G) > t0) --cf;
+    int np = 0;
+    for (int cc = cf; cc <= c; ++cc) {
+      const long long a0 = range_start(cc, I, G), a1 = range_start(cc + 1, I, G);
+      const long long p0 = a0 > t0 ? a0 : t0, p1 = a1 < t1 ? a1 : t1;
+      if (p0 >= p1) continue;
+      if (np == kMaxPieces) {          // more pieces than slots: cannot happen (see kCtasPerTile)
+        atomicOr(status, PI_STATUS_BAD_COUNT);
+        break;
+      }
+      slots_s[np++] = 2 * cc + (p0 == a0 ? 0 : 1);
+    }
+    nslot_s = np;
+  }
+  __syncthreads();
+  const int np = nslot_s;
+  const int q = threadIdx.x;
+  const int i = tile_row(idx, tile * kTile + q, count, ffn, status);
+  const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
+  auto fetch8 = [&](int col, float *v) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    for (int p0 = 0; p0 < np; p0 += 4) {     // four pieces' loads in flight, added in order
+      float t[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (p0 + u < np) {
+          const float *src = piece + ((size_t)slots_s[p0 + u] * ncolD + col) * kTile + q;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t[u][j] = src[(size_t)j * kTile];
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (p0 + u < np)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] += t[u][j];
+    }
+  };
+  const int c_begin = MODE == kLogits ? 0 : 8 * (int)blockIdx.y;
+  row_epilogue<MODE, REGLU>(fetch8, c_begin, c_begin + 8, i, tile * kTile + q, bi, B, Bp, Nmma, abuf, abuf_ld,
+                            mask_out);
 }
 
 // ---------------------------------------------------------------------------
@@ -540,37 +652,30 @@ bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// h = ReLU(sum of the K splits, in split order), written as the fp16 pair
-// (hi rows 0..Bp-1, lo rows Bp..2Bp-1) of the logits kernel's B operand.
-__global__ void k_hidden_finish(const float *__restrict__ part, int nsplit, int B, int Bp, int rank, int rpad,
-                                __half *__restrict__ hbuf) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  const int n = Bp * rpad;
-  if (e >= n) return;
-  const int b = e / rpad, row = e % rpad;
-  float acc = 0.f;
-  for (int k = 0; k < nsplit; ++k) acc += part[(size_t)k * n + e];
-  const float h = (b < B && row < rank && acc > 0.f) ? acc : 0.f;
-  const __half hi = __float2half_rn(h);
-  hbuf[e] = hi;
-  hbuf[(size_t)n + e] = __float2half_rn(h - __half2float(hi));
-}
-
 constexpr size_t kTcSmemBudget = 200 * 1024;
 
+// Launch k_tc_rows over nrows candidate rows (count_const, or *count on the
+// device when count is given) and then k_tc_fixup for the tiles it split.
+// rows_known: the row count is known here (the predictor), so the stage
+// width can be chosen to give every active CTA at least one stage; otherwise
+// the widest stage is taken (most contiguous bytes per gathered row).
 template <int MODE, bool REGLU>
 cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, const CUtensorMap &tm_x,
                         const int32_t *idx, const int32_t *count, int count_const, const float *bias, int K,
-                        int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, cudaStream_t s,
-                        int ksplit = 1, float *fout = nullptr) {
-  // K: row length; each of the ksplit CTAs of a row tile contracts K / ksplit
-  const int klen = K / ksplit;
+                        int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, float *piece,
+                        bool rows_known, cudaStream_t s) {
   const int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const size_t sub = NA * (size_t)kTile * 128 + (((size_t)Nmma * 128 + 1023) & ~(size_t)1023);
-  // widest stage (kw consecutive slabs per row) that divides K and keeps >= 2 stages
+  const int slabs = K / kSlab;
+  const long long tiles = (nrows + kTile - 1) / kTile;
+  const int G = L->num_sms;
+  // widest stage (kw consecutive slabs per row) that divides K and keeps >= 2
+  // stages; with a known row count, also >= G stages over all tiles
   int kw = 4;
-  while (kw > 1 && ((klen / kSlab) % kw != 0 || (kTcSmemBudget - 1024) / (kw * sub) < 2)) kw >>= 1;
+  while (kw > 1 && (slabs % kw != 0 || (kTcSmemBudget - 1024) / (kw * sub) < 2 ||
+                    (rows_known && tiles * (slabs / kw) < std::min<long long>(G, tiles * kCtasPerTile))))
+    kw >>= 1;
   const size_t stage = kw * sub;
   int ns = (int)((kTcSmemBudget - 1024) / stage);
   if (ns > 8) ns = 8;
@@ -579,10 +684,13 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   auto kern = k_tc_rows<MODE, REGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int grid = (nrows + kTile - 1) / kTile;
-  if (grid > L->num_sms) grid = L->num_sms;
-  kern<<<dim3(grid, ksplit), 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, klen, nrows, B, Bp,
-                                             ns, kw, out, fout, out_ld, mask, L->status);
+  kern<<<G, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, kw, out, out_ld,
+                            piece, mask, L->status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const dim3 fgrid(G, MODE == kLogits ? 1 : Bp / 8);
+  k_tc_fixup<MODE, REGLU><<<fgrid, 128, 0, s>>>(piece, idx, count, count_const, bias, nrows, B, Bp, slabs / kw, G,
+                                                out, out_ld, mask, L->status);
   return cudaGetLastError();
 }
 
@@ -604,36 +712,26 @@ bool tc_predict_supported(const pi_layer *L, int B) {
 
 int tc_rank_pad(const pi_layer *L) { return (L->rank + kTile - 1) / kTile * kTile; }
 
-int tc_hidden_splits(const pi_layer *L) {
-  const int tiles = tc_rank_pad(L) / kTile, slabs = L->d / kSlab;
-  int k = std::min(kMaxHiddenSplits, std::max(1, L->num_sms / tiles));
-  while (k > 1 && slabs % k != 0) --k;
-  return k;
+size_t tc_piece_bytes(const pi_layer *L, int B) {
+  // two slots per CTA of 128 rows x (at most 2 Bp) fp32 accumulator columns
+  return sizeof(float) * 2 * (size_t)L->num_sms * kTile * 2 * (size_t)tc_bpad(B);
 }
 
 cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
-                           float *hpart, cudaStream_t s) {
+                           float *piece, cudaStream_t s) {
   const int Bp = tc_bpad(B);
   const int rpad = tc_rank_pad(L);
   CUtensorMap tm_x, tm_h;
   if (!encode_2d(&tm_x, x, L->d, B, (uint64_t)L->d * 2, kSlab, Bp) ||
       !encode_2d(&tm_h, hbuf, rpad, 2 * Bp, (uint64_t)rpad * 2, kSlab, 2 * Bp))
     return cudaErrorInvalidValue;
-  // h = ReLU(W_p1 x) as an fp16 pair (K split over CTAs, splits added in
-  // order), then l = W_p2 h + c_p -> union mask
-  const int ks = tc_hidden_splits(L);
-  cudaError_t e = launch_rows<kHiddenPart, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr,
-                                                  L->d, L->rank, B, Bp, nullptr, rpad, nullptr, s, ks, hpart);
-  if (e != cudaSuccess) return e;
-  const int n = Bp * rpad;
-  k_hidden_finish<<<(n + 255) / 256, 256, 0, s>>>(hpart, ks, B, Bp, L->rank, rpad, hbuf);
-  e = cudaGetLastError();
+  // h = ReLU(W_p1 x) as an fp16 pair, then l = W_p2 h + c_p -> union mask
+  cudaError_t e = launch_rows<kHidden, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr, L->d,
+                                              rpad, B, Bp, hbuf, rpad, nullptr, piece, true, s);
   if (e != cudaSuccess) return e;
   return launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->ffn, B,
-                                     Bp, nullptr, 0, mask_union, s);
+                                     Bp, nullptr, 0, mask_union, piece, true, s);
 }
-
-
 
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,
@@ -651,10 +749,11 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
 
   cudaError_t e = record_hook(L->ev_before, s);
   if (e != cudaSuccess) return e;
-  e = reglu ? launch_rows<kAct, true>(L, reglu ? L->W_gate : L->W_up, L->W_up, tm_x, idx, count, count_const, L->b,
-                                      L->d, L->ffn, B, Bp, abuf, ffn_pad, nullptr, s)
+  float *piece = reinterpret_cast<float *>(ws + w.tcpart);
+  e = reglu ? launch_rows<kAct, true>(L, L->W_gate, L->W_up, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
+                                      Bp, abuf, ffn_pad, nullptr, piece, false, s)
             : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
-                                       Bp, abuf, ffn_pad, nullptr, s);
+                                       Bp, abuf, ffn_pad, nullptr, piece, false, s);
   if (e != cudaSuccess) return e;
 
   // down: stages of cw x 16 KB gathered W_down^T + the [a_hi; a_lo] slab
