@@ -181,6 +181,7 @@ WsLayout ws_layout(const pi_layer *L, int B) {
   w.abuf = off;    off += align_up(2 * sizeof(__half) * (size_t)tc_bpad(B) * tc_ffn_pad(L));
   w.hbuf = off;    off += align_up(2 * sizeof(__half) * (size_t)tc_bpad(B) * tc_rank_pad(L));
   w.tcpart = off;  off += B >= 3 ? align_up(tc_piece_bytes(L, B)) : 0;
+  w.tcnt = off;    off += B >= 3 ? align_up(sizeof(int32_t) * (size_t)(tc_ffn_pad(L) / 128)) : 0;
   w.total = off;
   return w;
 }
@@ -455,12 +456,14 @@ pi_status pi_layer_forward(pi_layer *L, const uint16_t *x, int32_t B, int32_t *i
     return PI_OK;
   }
   uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
-  if (pi::tc_predict_supported(L, B))
+  if (pi::tc_predict_supported(L, B)) {
     PI_TRY_CUDA(pi::run_predict_tc(L, xh, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
-                                    reinterpret_cast<float *>(wsb + w.tcpart), s));
-  else
+                                    reinterpret_cast<float *>(wsb + w.tcpart),
+                                    reinterpret_cast<int32_t *>(wsb + w.tcnt), idx, count, s));
+  } else {
     PI_TRY_CUDA(pi::run_predict(L, xh, B, mask, nullptr, reinterpret_cast<float *>(wsb + w.h), s, true));
-  PI_TRY_CUDA(pi::run_compact(L, mask, 1, idx, count, s));
+    PI_TRY_CUDA(pi::run_compact(L, mask, 1, idx, count, s));
+  }
   PI_TRY_CUDA(pi::run_sparse_ffn(L, xh, B, idx, count, 0, y, w, wsb, s));
   return PI_OK;
 }
@@ -502,12 +505,15 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
   for (int l = 0; l < n_layers; ++l) {
     pi_layer *Ll = layers[l];
     uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
-    if (pi::tc_predict_supported(Ll, B))
+    if (pi::tc_predict_supported(Ll, B)) {
       PI_TRY_CUDA(pi::run_predict_tc(Ll, xh + l * xs, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
-                                      reinterpret_cast<float *>(wsb + w.tcpart), s));
-    else
+                                      reinterpret_cast<float *>(wsb + w.tcpart),
+                                      reinterpret_cast<int32_t *>(wsb + w.tcnt), idx + (size_t)l * L->ffn,
+                                      count + l, s));
+    } else {
       PI_TRY_CUDA(pi::run_predict(Ll, xh + l * xs, B, mask, nullptr, reinterpret_cast<float *>(wsb + w.h), s, true));
-    PI_TRY_CUDA(pi::run_compact(Ll, mask, 1, idx + (size_t)l * L->ffn, count + l, s));
+      PI_TRY_CUDA(pi::run_compact(Ll, mask, 1, idx + (size_t)l * L->ffn, count + l, s));
+    }
     PI_TRY_CUDA(pi::run_sparse_ffn(Ll, xh + l * xs, B, idx + (size_t)l * L->ffn, count + l, 0,
                                    y + l * xs, w, wsb, s));
   }

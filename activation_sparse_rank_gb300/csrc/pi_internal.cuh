@@ -58,6 +58,7 @@ struct WsLayout {
   size_t abuf = 0;     // fp16 [2*Bp, ffn_pad]  activations (hi; lo) of the tensor-core path
   size_t hbuf = 0;     // fp16 [2*Bp, rank_pad] predictor hidden layer (hi; lo), tensor-core path
   size_t tcpart = 0;   // float [2 G, 2 Bp, 128] tensor-core tiles split between CTAs
+  size_t tcnt = 0;     // int32 [ffn_pad / 128] active rows per logits tile
   size_t total = 0;
 };
 
@@ -141,10 +142,11 @@ int tc_bpad(int B);
 int tc_ffn_pad(const pi_layer *L);
 bool tc_predict_supported(const pi_layer *L, int B);
 int tc_rank_pad(const pi_layer *L);
-// h (fp16 pair, in hbuf [2Bp, rank_pad]) and the batch-union mask [ffn] on the
-// tensor cores; piece: fp32 scratch of tc_piece_bytes for tiles split between CTAs.
+// h (fp16 pair, in hbuf [2Bp, rank_pad]), the batch-union mask [ffn] and its
+// ascending list idx / count on the tensor cores; piece: fp32 scratch of
+// tc_piece_bytes for tiles split between CTAs; tile_cnt: int [ffn_pad / 128].
 cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
-                           float *piece, cudaStream_t s);
+                           float *piece, int32_t *tile_cnt, int32_t *idx, int32_t *count, cudaStream_t s);
 size_t tc_piece_bytes(const pi_layer *L, int B);
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,

@@ -13,18 +13,21 @@
 // a = a_hi + a_lo (stacked as 2*Bp columns), which keeps their rounding error
 // near 2^-22 relative instead of fp16's 2^-11.
 //
-// k_tc_up:   persistent CTAs over 128-neuron tiles of the active list.  Per
-//            64-element K slab, all 128 threads gather the 128 rows with
-//            16-byte cp.async copies written straight into the 128-byte
-//            swizzled operand layout (a gathered row piece is only 128 bytes,
-//            too small for TMA to move at full rate), TMA loads the x slab,
-//            and thread 0 issues the MMAs of a multi-stage mbarrier pipeline;
-//            four warps then read the accumulators from TMEM.
-// k_tc_down: CTA (column tile of 128, split of the list).  Per 64-neuron slab,
-//            the threads gather 64 rows x 128 columns of W_down^T (MN-major
-//            operand) the same way and TMA loads the matching [a_hi; a_lo]
-//            slab; partial sums go to the workspace and k_reduce adds them
-//            in split order (deterministic).
+// k_tc_rows: the up rows (and the predictor's two layers), 128-row tiles of
+//            the list.  Per stage of kw 64-element K slabs, all 128 threads
+//            gather the 128 rows with 16-byte cp.async copies written
+//            straight into the 128-byte swizzled operand layout (a gathered
+//            row piece is only 128-512 bytes, too small for TMA to move at
+//            full rate), TMA loads the x slab, and thread 0 issues the MMAs
+//            of a multi-stage mbarrier pipeline; four warps then read the
+//            accumulators from TMEM.
+// k_tc_down: per 64-neuron slab, the threads gather 64 rows x cw * 128
+//            columns of W_down^T (MN-major operand) the same way and TMA
+//            loads the matching [a_hi; a_lo] slab.
+// Both split their (tile, K stage) work stream-K style over all SMs: each CTA
+// takes an equal contiguous share, so no SM idles when the tile count is not
+// a multiple of the SM count; tiles shared by several CTAs are summed from
+// per-CTA pieces in CTA order (deterministic; no float atomics).
 // All mbarrier waits are bounded; on a timeout the kernel sets a status bit,
 // waits (bounded) for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
@@ -184,11 +187,11 @@ __device__ __forceinline__ int tile_row(const int32_t *idx, int k, int count, in
 // column kq).  fetch8(c, v) yields D columns c .. c+7 of the row; for kAct
 // and kHidden only token columns [c_begin, c_end) are produced.
 template <int MODE, bool REGLU, typename F>
-__device__ __forceinline__ void row_epilogue(F fetch8, int c_begin, int c_end, int i, int kq, float bi, int B,
+__device__ __forceinline__ bool row_epilogue(F fetch8, int c_begin, int c_end, int i, int kq, float bi, int B,
                                              int Bp, int Nmma, __half *abuf, int abuf_ld, uint8_t *mask_out) {
-  if (MODE == kLogits) {
+  if (MODE == kLogits) {                // kLogits: token columns [c_begin, c_end); returns l > 0 for one of them
     bool on = false;
-    for (int c0 = 0; c0 < Bp; c0 += 8) {
+    for (int c0 = c_begin; c0 < c_end; c0 += 8) {
       float hi8[8], lo8[8];
       fetch8(c0, hi8);
       fetch8(Bp + c0, lo8);
@@ -196,7 +199,8 @@ __device__ __forceinline__ void row_epilogue(F fetch8, int c_begin, int c_end, i
       for (int j = 0; j < 8; ++j)
         if (c0 + j < B) on |= (hi8[j] + lo8[j] + bi) > 0.f;
     }
-    if (i >= 0) mask_out[i] = on ? 1 : 0;
+    if (i >= 0 && mask_out) mask_out[i] = on ? 1 : 0;
+    return on;
   } else {
     for (int c0 = c_begin; c0 < c_end; c0 += 8) {
       float g8[8], u8[8];
@@ -216,6 +220,7 @@ __device__ __forceinline__ void row_epilogue(F fetch8, int c_begin, int c_end, i
         abuf[(size_t)(Bp + b) * abuf_ld + kq] = lo;
       }
     }
+    return false;
   }
 }
 
@@ -227,7 +232,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
                                                     int count_const, const float *__restrict__ bias, int d, int ffn,
                                                     int B, int Bp, int nstage, int kw, __half *__restrict__ abuf,
                                                     int abuf_ld, float *__restrict__ piece,
-                                                    uint8_t *__restrict__ mask_out, unsigned int *status) {
+                                                    uint8_t *__restrict__ mask_out, int32_t *__restrict__ tile_cnt,
+                                                    unsigned int *status) {
   // d: row length of W and contraction length K; ffn: number of rows of W.
   // A pipeline stage holds kw consecutive 64-element K slabs, so every
   // gathered row contributes kw * 128 contiguous bytes per stage.
@@ -370,8 +376,12 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
     if (whole) {
       const int i = rows_s[q];
       const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
-      row_epilogue<MODE, REGLU>([&](int c, float *v) { tmem_ld8(trow + (uint32_t)c, v); }, 0, Bp, i, k0 + q, bi, B,
-                                Bp, Nmma, abuf, abuf_ld, mask_out);
+      const bool on = row_epilogue<MODE, REGLU>([&](int c, float *v) { tmem_ld8(trow + (uint32_t)c, v); }, 0, Bp,
+                                                i, k0 + q, bi, B, Bp, Nmma, abuf, abuf_ld, mask_out);
+      if (MODE == kLogits) {            // active rows of the tile, for the ordered compaction
+        const int n_on = __syncthreads_count(on && i >= 0);
+        if (tid == 0) tile_cnt[tile] = n_on;
+      }
     } else {
       float *dst = piece + (size_t)slot * ncolD * kTile + q;
       for (int c0 = 0; c0 < ncolD; c0 += 8) {
@@ -395,14 +405,16 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
 
 // Tiles that k_tc_rows split between CTAs: block c finishes the tile whose
 // last stage lies in CTA c's range when that tile started in an earlier CTA's
-// range.  It adds the tile's pieces in CTA order and applies the epilogue to
-// token columns [8 * blockIdx.y, +8) (kLogits: all columns, one y block).
+// range.  It adds the tile's pieces in CTA order and applies the epilogue;
+// the block has 128 threads per group of token columns (thread = tile row),
+// so each thread adds only its group's columns of the pieces.
 template <int MODE, bool REGLU>
-__global__ void __launch_bounds__(128) k_tc_fixup(const float *__restrict__ piece, const int32_t *__restrict__ idx,
-                                                  const int32_t *__restrict__ count_p, int count_const,
-                                                  const float *__restrict__ bias, int ffn, int B, int Bp, int KT, int grid,
-                                                  __half *__restrict__ abuf, int abuf_ld,
-                                                  uint8_t *__restrict__ mask_out, unsigned int *status) {
+__global__ void __launch_bounds__(1024) k_tc_fixup(const float *__restrict__ piece, const int32_t *__restrict__ idx,
+                                                   const int32_t *__restrict__ count_p, int count_const,
+                                                   const float *__restrict__ bias, int ffn, int B, int Bp, int KT,
+                                                   int grid, __half *__restrict__ abuf, int abuf_ld,
+                                                   uint8_t *__restrict__ mask_out, int32_t *__restrict__ tile_cnt,
+                                                   unsigned int *status) {
   constexpr int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const int ncolD = NA * Nmma;
@@ -419,6 +431,7 @@ __global__ void __launch_bounds__(128) k_tc_fixup(const float *__restrict__ piec
   if (re < t1) return;                           // the tile goes on in a later CTA
   __shared__ int slots_s[kMaxPieces];
   __shared__ int nslot_s;
+  __shared__ unsigned char on_s[8][kTile];
   if (threadIdx.x == 0) {          // the tile's pieces, in CTA order
     int cf = c;
     while (cf > 0 && range_start(cf, I, G) > t0) --cf;
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__(128) k_tc_fixup(const float *__restrict__ piec
   }
   __syncthreads();
   const int np = nslot_s;
-  const int q = threadIdx.x;
+  const int q = threadIdx.x % kTile, grp = threadIdx.x / kTile, ngrp = blockDim.x / kTile;
   const int i = tile_row(idx, tile * kTile + q, count, ffn, status);
   const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
   auto fetch8 = [&](int col, float *v) {
@@ -459,9 +472,48 @@ __global__ void __launch_bounds__(128) k_tc_fixup(const float *__restrict__ piec
           for (int j = 0; j < 8; ++j) v[j] += t[u][j];
     }
   };
-  const int c_begin = MODE == kLogits ? 0 : 8 * (int)blockIdx.y;
-  row_epilogue<MODE, REGLU>(fetch8, c_begin, c_begin + 8, i, tile * kTile + q, bi, B, Bp, Nmma, abuf, abuf_ld,
-                            mask_out);
+  bool on = false;
+  for (int c0 = 8 * grp; c0 < Bp; c0 += 8 * ngrp)
+    on |= row_epilogue<MODE, REGLU>(fetch8, c0, c0 + 8, i, tile * kTile + q, bi, B, Bp, Nmma, abuf, abuf_ld,
+                                    nullptr);
+  if (MODE == kLogits) {
+    on_s[grp][q] = on ? 1 : 0;
+    __syncthreads();
+    bool any = false;
+    if (grp == 0) {
+      for (int g2 = 0; g2 < ngrp; ++g2) any |= on_s[g2][q] != 0;
+      if (i >= 0) mask_out[i] = any ? 1 : 0;
+    }
+    const int n_on = __syncthreads_count(grp == 0 && any && i >= 0);
+    if (threadIdx.x == 0) tile_cnt[tile] = n_on;
+  }
+}
+
+// Ordered compaction from the logits kernels' per-tile counts: block t writes
+// the active rows of tile t (ascending) after the sum of the counts of the
+// tiles before it; the last block writes the total.
+__global__ void __launch_bounds__(kTile) k_compact_tiles(const uint8_t *__restrict__ mask,
+                                                         const int32_t *__restrict__ tile_cnt, int ffn,
+                                                         int32_t *__restrict__ idx, int32_t *__restrict__ count) {
+  __shared__ int red_s[4];
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int pre = 0;
+  for (int k = tid; k < t; k += kTile) pre += tile_cnt[k];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
+  const int row = t * kTile + tid;
+  const bool on = row < ffn && mask[row] != 0;
+  const unsigned bal = __ballot_sync(0xffffffffu, on);
+  if (lane == 0) red_s[w] = pre;
+  __syncthreads();
+  const int base = red_s[0] + red_s[1] + red_s[2] + red_s[3];
+  __syncthreads();
+  if (lane == 0) red_s[w] = __popc(bal);
+  __syncthreads();
+  int wpre = 0;
+  for (int k = 0; k < w; ++k) wpre += red_s[k];
+  if (on) idx[base + wpre + __popc(bal & ((1u << lane) - 1u))] = row;
+  if (t == gridDim.x - 1 && tid == 0) *count = base + red_s[0] + red_s[1] + red_s[2] + red_s[3];
 }
 
 // ---------------------------------------------------------------------------
@@ -469,9 +521,14 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
                                                     const __grid_constant__ CUtensorMap tm_a,   // abuf, box 64 x 2Bp
                                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
                                                     int count_const, int d, int ffn, int B, int Bp, int nstage,
-                                                    int cw, float *__restrict__ partial, unsigned int *status) {
-  // A CTA owns cw column tiles of 128 (cw * 256 contiguous bytes of every
-  // gathered W_down^T row per slab), one TMEM accumulator per tile.
+                                                    int cw, float *__restrict__ piece, unsigned int *status) {
+  // Work units are (column tile of cw * 128 outputs, 64-row slab of the
+  // list), column-tile major, split stream-K style over the CTAs: each CTA
+  // accumulates its consecutive slabs of one column tile in TMEM (cw * 256
+  // contiguous bytes of every gathered W_down^T row per slab) and writes the
+  // sum as one fp32 piece [B, cw * 128] to slot 2c (its first piece) or
+  // 2c + 1 (its last); k_tc_down_reduce adds each column tile's pieces in CTA
+  // order.
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   const int N2 = 2 * Bp;
@@ -480,12 +537,12 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
   const uint32_t slabW = (uint32_t)cw * tileW;
   const uint32_t slabA = (uint32_t)N2 * 128;
   const uint32_t stage_bytes = slabW + ((slabA + 1023) & ~1023u);
+  const int CW = cw * kTile;                              // outputs per column tile
   __shared__ __align__(8) unsigned long long full_s[8], empty_s[8], done_s;
   __shared__ uint32_t taddr_s;
   __shared__ int fail_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j0 = blockIdx.x * kTile * cw;
   const int ncols = tmem_cols_for(cw * N2);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
@@ -506,19 +563,27 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
   const uint32_t tmem = taddr_s;
 
   int count = count_p ? *count_p : count_const;
-  if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;     // flagged by k_tc_up
+  if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;     // flagged by the up kernel
   const int KS = (count + kSlab - 1) / kSlab;
-  const int per = (KS + gridDim.y - 1) / gridDim.y;
-  const int ks0 = min(KS, (int)blockIdx.y * per), ks1 = min(KS, ks0 + per);
-  const int nk = ks1 - ks0;
+  const int ctiles = (d + CW - 1) / CW;
+  const long long I = (long long)ctiles * KS;
+  const int G = active_ctas(gridDim.x, ctiles), cta = blockIdx.x;
+  const long long rs = cta < G ? range_start(cta, I, G) : 0, re = cta < G ? range_start(cta + 1, I, G) : 0;
   const uint32_t idesc = idesc_f16(N2, kTile, true);
+  // Every thread copies 16 of the 2048 16-byte chunks of a slab: chunk
+  // c = tid % 8 of column half (tid / 8) % 2 of rows tid / 16 + 8 i, into the
+  // MN-major swizzled layout (8 rows of 128 bytes per 1024-byte group);
+  // thread 0 also loads the [a_hi; a_lo] slab by TMA and issues the MMAs.
+  const int cch = tid & 7, hh = (tid >> 3) & 1, r0 = tid >> 4;
+  uint32_t gpos = 0, done_phase = 0;
 
-  if (nk > 0) {
-    // Every thread copies 16 of the 2048 16-byte chunks of a slab: chunk
-    // c = tid % 8 of column half (tid / 8) % 2 of rows tid / 16 + 8 i, into the
-    // MN-major swizzled layout (8 rows of 128 bytes per 1024-byte group);
-    // thread 0 also loads the [a_hi; a_lo] slab by TMA and issues the MMAs.
-    const int cch = tid & 7, hh = (tid >> 3) & 1, r0 = tid >> 4;
+  for (long long s0 = rs; s0 < re;) {
+    const int tile = (int)(s0 / KS);
+    const int kb = (int)(s0 % KS);
+    const int n = (int)min((long long)(KS - kb), re - s0);   // slabs of this piece
+    const int slot = 2 * cta + (s0 == rs ? 0 : 1);
+    s0 += n;
+    const int j0 = tile * CW;
     // row indices of the next slab to issue, loaded one issue ahead so their
     // latency hides behind the copies of the current slab
     int nxt[8];
@@ -530,17 +595,18 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
         nxt[i] = (rid >= 0 && rid < ffn) ? rid : 0;  // padding / invalid: row 0 times a zero activation
       }
     };
-    load_rows(ks0);
-    auto issue = [&](int t) {
-      const int s = t % nstage;
-      if (t >= nstage && !mb_wait(su32(&empty_s[s]), ((t / nstage) - 1) & 1)) fail_s = 1;
+    load_rows(kb);
+    auto issue = [&](int it) {
+      const uint32_t g = gpos + (uint32_t)it;
+      const int s = (int)(g % (uint32_t)nstage);
+      if (g >= (uint32_t)nstage && !mb_wait(su32(&empty_s[s]), ((g / nstage) - 1) & 1)) fail_s = 1;
       unsigned char *st = sm + (size_t)s * stage_bytes;
       const uint32_t bar = su32(&full_s[s]);
-      const int slab = ks0 + t;
+      const int slab = kb + it;
       int cur[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
-      if (t + 1 < nk) load_rows(slab + 1);
+      if (it + 1 < n) load_rows(slab + 1);
       for (int c = 0; c < cw; ++c) {
         const uint32_t base = su32(st) + c * tileW + hh * half_bytes;
         const int col = j0 + c * kTile + hh * 64 + cch * 8;
@@ -557,14 +623,15 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
         tma_tile2d(su32(st + slabW), &tm_a, slab * kSlab, 0, bar);
       }
     };
-    const int pre = min(nstage - 1, nk);
-    for (int t = 0; t < pre; ++t) issue(t);
-    for (int t = 0; t < nk; ++t) {
+    const int pre = min(nstage - 1, n);
+    for (int it = 0; it < pre; ++it) issue(it);
+    for (int it = 0; it < n; ++it) {
       if (fail_s) break;
-      if (t + nstage - 1 < nk) issue(t + nstage - 1);
+      if (it + nstage - 1 < n) issue(it + nstage - 1);
       if (tid == 0) {
-        const int s = t % nstage;
-        if (!mb_wait(su32(&full_s[s]), (t / nstage) & 1)) {
+        const uint32_t g = gpos + (uint32_t)it;
+        const int s = (int)(g % (uint32_t)nstage);
+        if (!mb_wait(su32(&full_s[s]), (g / nstage) & 1)) {
           fail_s = 1;
         } else {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -576,47 +643,72 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
               // A: MN-major (K groups of 8 rows at 1024 B, column halves at half_bytes)
               const uint64_t ad = sdesc(su32(st) + c * tileW + kk * 16 * 128, half_bytes, 1024);
               const uint64_t bd = sdesc(su32(st + slabW) + kk * 32, 16, 1024);
-              mma_f16(tmem + (uint32_t)(c * N2), ad, bd, idesc, (t | kk) ? 1u : 0u);
+              mma_f16(tmem + (uint32_t)(c * N2), ad, bd, idesc, (it | kk) ? 1u : 0u);
             }
           mma_commit(su32(&empty_s[s]));
         }
       }
     }
+    gpos += (uint32_t)n;
     if (tid == 0) mma_commit(su32(&done_s));
-  }
-  __syncthreads();
-  if (nk > 0 && !fail_s) {
-    if (!mb_wait(su32(&done_s), 0)) fail_s = 1;
-  }
-  __syncthreads();
-  if (!fail_s) {
+    __syncthreads();
+    if (fail_s) break;
+    if (!mb_wait(su32(&done_s), done_phase)) { fail_s = 1; break; }
+    done_phase ^= 1u;
     asm volatile("tcgen05.fence::after_thread_sync;");
     for (int c = 0; c < cw; ++c) {
-      const int j = j0 + c * kTile + warp * 32 + lane;   // TMEM lane = output column
+      const int jl = c * kTile + warp * 32 + lane;           // TMEM lane = output column
       const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * N2);
+      float *dst = piece + (size_t)slot * B * CW + jl;
       for (int c0 = 0; c0 < Bp; c0 += 8) {
         float hi[8], lo[8];
-        if (nk > 0) {
-          tmem_ld8(trow + (uint32_t)c0, hi);
-          tmem_ld8(trow + (uint32_t)(Bp + c0), lo);
-        } else {
+        tmem_ld8(trow + (uint32_t)c0, hi);
+        tmem_ld8(trow + (uint32_t)(Bp + c0), lo);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) hi[q] = lo[q] = 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int b = c0 + q;
-          if (b < B && j < d) partial[((size_t)blockIdx.y * B + b) * d + j] = hi[q] + lo[q];
-        }
+        for (int q = 0; q < 8; ++q)
+          if (c0 + q < B) dst[(size_t)(c0 + q) * CW] = hi[q] + lo[q];
       }
     }
-  } else if (tid == 0) {
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+  }
+  if (fail_s && tid == 0) {
     atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
     for (int s = 0; s < nstage; ++s) mb_wait(su32(&full_s[s]), 0), mb_wait(su32(&full_s[s]), 1);
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
+}
+
+// y[b, j] = the pieces of j's column tile added in CTA order (0 for an empty list).
+__global__ void k_tc_down_reduce(const float *__restrict__ piece, const int32_t *__restrict__ count_p,
+                                 int count_const, int d, int ffn, int B, int CW, int grid, float *__restrict__ y) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= B * d) return;
+  const int b = e / d, j = e % d;
+  int count = count_p ? *count_p : count_const;
+  if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;
+  const long long KS = (count + kSlab - 1) / kSlab;
+  const int ctiles = (d + CW - 1) / CW;
+  const long long I = (long long)ctiles * KS;
+  const int G = active_ctas(grid, ctiles);
+  const int tile = j / CW, jl = j % CW;
+  const long long t0 = tile * KS, t1 = t0 + KS;
+  float acc = 0.f;
+  if (KS > 0) {
+    // CTA holding iteration x: the largest c with c * I / G <= x
+    const int cf = (int)(((t0 + 1) * G + I - 1) / I) - 1;
+    const int cl = (int)((t1 * G + I - 1) / I) - 1;
+    for (int cc = cf; cc <= cl; ++cc) {
+      const long long a0 = range_start(cc, I, G), a1 = range_start(cc + 1, I, G);
+      const long long p0 = a0 > t0 ? a0 : t0, p1 = a1 < t1 ? a1 : t1;
+      if (p0 >= p1) continue;
+      const int slot = 2 * cc + (p0 == a0 ? 0 : 1);
+      acc += piece[((size_t)slot * B + b) * CW + jl];
+    }
+  }
+  y[e] = acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -663,7 +755,7 @@ template <int MODE, bool REGLU>
 cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, const CUtensorMap &tm_x,
                         const int32_t *idx, const int32_t *count, int count_const, const float *bias, int K,
                         int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, float *piece,
-                        bool rows_known, cudaStream_t s) {
+                        int32_t *tile_cnt, bool rows_known, cudaStream_t s) {
   const int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const size_t sub = NA * (size_t)kTile * 128 + (((size_t)Nmma * 128 + 1023) & ~(size_t)1023);
@@ -685,12 +777,12 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<G, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, kw, out, out_ld,
-                            piece, mask, L->status);
+                            piece, mask, tile_cnt, L->status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 fgrid(G, MODE == kLogits ? 1 : Bp / 8);
-  k_tc_fixup<MODE, REGLU><<<fgrid, 128, 0, s>>>(piece, idx, count, count_const, bias, nrows, B, Bp, slabs / kw, G,
-                                                out, out_ld, mask, L->status);
+  const int groups = std::min(Bp / 8, 8);       // 128 threads per group of token columns
+  k_tc_fixup<MODE, REGLU><<<G, kTile * groups, 0, s>>>(piece, idx, count, count_const, bias, nrows, B, Bp,
+                                                       slabs / kw, G, out, out_ld, mask, tile_cnt, L->status);
   return cudaGetLastError();
 }
 
@@ -718,7 +810,7 @@ size_t tc_piece_bytes(const pi_layer *L, int B) {
 }
 
 cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
-                           float *piece, cudaStream_t s) {
+                           float *piece, int32_t *tile_cnt, int32_t *idx, int32_t *count, cudaStream_t s) {
   const int Bp = tc_bpad(B);
   const int rpad = tc_rank_pad(L);
   CUtensorMap tm_x, tm_h;
@@ -726,11 +818,15 @@ cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *m
       !encode_2d(&tm_h, hbuf, rpad, 2 * Bp, (uint64_t)rpad * 2, kSlab, 2 * Bp))
     return cudaErrorInvalidValue;
   // h = ReLU(W_p1 x) as an fp16 pair, then l = W_p2 h + c_p -> union mask
+  // and per-tile counts, then the ordered list of active neurons
   cudaError_t e = launch_rows<kHidden, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr, L->d,
-                                              rpad, B, Bp, hbuf, rpad, nullptr, piece, true, s);
+                                              rpad, B, Bp, hbuf, rpad, nullptr, piece, nullptr, true, s);
   if (e != cudaSuccess) return e;
-  return launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->ffn, B,
-                                     Bp, nullptr, 0, mask_union, piece, true, s);
+  e = launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->ffn, B,
+                                  Bp, nullptr, 0, mask_union, piece, tile_cnt, true, s);
+  if (e != cudaSuccess) return e;
+  k_compact_tiles<<<(L->ffn + kTile - 1) / kTile, kTile, 0, s>>>(mask_union, tile_cnt, L->ffn, idx, count);
+  return cudaGetLastError();
 }
 
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
@@ -740,7 +836,7 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   const int Bp = tc_bpad(B);
   const int ffn_pad = tc_ffn_pad(L);
   __half *abuf = reinterpret_cast<__half *>(ws + w.abuf);
-  float *partial = reinterpret_cast<float *>(ws + w.partial);
+  float *piece = reinterpret_cast<float *>(ws + w.tcpart);   // split tiles of the up and down kernels
   CUtensorMap tm_x, tm_a;
   const uint64_t row_bytes = (uint64_t)L->d * 2;
   if (!encode_2d(&tm_x, x, L->d, B, row_bytes, kSlab, Bp) ||
@@ -749,11 +845,10 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
 
   cudaError_t e = record_hook(L->ev_before, s);
   if (e != cudaSuccess) return e;
-  float *piece = reinterpret_cast<float *>(ws + w.tcpart);
   e = reglu ? launch_rows<kAct, true>(L, L->W_gate, L->W_up, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
-                                      Bp, abuf, ffn_pad, nullptr, piece, false, s)
+                                      Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s)
             : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
-                                       Bp, abuf, ffn_pad, nullptr, piece, false, s);
+                                       Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s);
   if (e != cudaSuccess) return e;
 
   // down: stages of cw x 16 KB gathered W_down^T + the [a_hi; a_lo] slab
@@ -765,17 +860,16 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   const size_t dn_smem = 1024 + dn_ns * dn_stage;
   e = cudaFuncSetAttribute(k_tc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
   if (e != cudaSuccess) return e;
-  const int ctiles = (L->d + cw * kTile - 1) / (cw * kTile);
-  int nsplit = L->num_sms / ctiles;
-  if (nsplit < 1) nsplit = 1;
-  dim3 grid_dn(ctiles, nsplit);
-  k_tc_down<<<grid_dn, 128, dn_smem, s>>>(L->W_dT, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns, cw,
-                                         partial, L->status);
+  k_tc_down<<<L->num_sms, 128, dn_smem, s>>>(L->W_dT, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns,
+                                             cw, piece, L->status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = record_hook(L->ev_after, s);
   if (e != cudaSuccess) return e;
-  return run_reduce(partial, nsplit, B * L->d, y, s);
+  const int n = B * L->d;
+  k_tc_down_reduce<<<(n + 255) / 256, 256, 0, s>>>(piece, count, count_const, L->d, L->ffn, B, cw * kTile,
+                                                   L->num_sms, y);
+  return cudaGetLastError();
 }
 
 }  // namespace pi
