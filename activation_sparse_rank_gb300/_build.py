@@ -21,7 +21,7 @@ OUT = Path(os.environ.get("PI_BUILD_DIR", str(PKG / "_lib")))
 LIB = OUT / "libpi.so"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--split-compile=0",
          "--expt-relaxed-constexpr", "-I", str(INCLUDE), "-I", str(CSRC)]
 
 

@@ -30,6 +30,8 @@ PI_OK = 0
 PI_ACT_RELU = 0
 PI_ACT_REGLU = 1
 PI_MAX_BATCH = 128
+PI_ROWS_FP16 = 0
+PI_ROWS_FP8_E4M3 = 1
 
 _p = C.c_void_p
 _i32 = C.c_int32
@@ -38,7 +40,7 @@ _i32 = C.c_int32
 class pi_layer_desc(C.Structure):
     _fields_ = [("d", _i32), ("ffn", _i32), ("rank", _i32), ("act", _i32),
                 ("W_up", _p), ("W_gate", _p), ("b", _p), ("W_down", _p),
-                ("W_p1", _p), ("W_p2", _p), ("c_p", _p)]
+                ("W_p1", _p), ("W_p2", _p), ("c_p", _p), ("row_format", _i32)]
 
 
 _SIG = {
@@ -46,6 +48,7 @@ _SIG = {
     "pi_layer_destroy": (C.c_int, [_p]),
     "pi_layer_info": (C.c_int, [_p, _p, _p, _p, _p]),
     "pi_layer_perm": (C.c_int, [_p, _p]),
+    "pi_layer_rows_fp8": (C.c_int, [_p, _i32, _p, _p, _p]),
     "pi_workspace_bytes": (C.c_size_t, [_p, _i32]),
     "pi_predict": (C.c_int, [_p, _p, _i32, _p, _p, _p, C.c_size_t, _p]),
     "pi_compact_active": (C.c_int, [_p, _p, _i32, _p, _p, _p]),
@@ -104,7 +107,7 @@ def _req(t: torch.Tensor, dtype, name: str):
     return t
 
 
-def make_desc(W_up, W_gate, b, W_down, W_p1, W_p2, c_p, act) -> pi_layer_desc:
+def make_desc(W_up, W_gate, b, W_down, W_p1, W_p2, c_p, act, rows="fp16") -> pi_layer_desc:
     act_id = PI_ACT_REGLU if act in ("reglu", PI_ACT_REGLU) else PI_ACT_RELU
     _req(W_up, torch.float16, "W_up")
     ffn, d = W_up.shape
@@ -116,18 +119,21 @@ def make_desc(W_up, W_gate, b, W_down, W_p1, W_p2, c_p, act) -> pi_layer_desc:
         _req(W_gate, torch.float16, "W_gate")
     if c_p is not None:
         _req(c_p, torch.float32, "c_p")
+    if rows not in ("fp16", "fp8"):
+        raise ValueError(f"rows must be 'fp16' or 'fp8', not {rows!r}")
     return pi_layer_desc(d, ffn, rank, act_id, W_up.data_ptr(),
                          None if W_gate is None else W_gate.data_ptr(), b.data_ptr(),
                          W_down.data_ptr(), W_p1.data_ptr(), W_p2.data_ptr(),
-                         None if c_p is None else c_p.data_ptr())
+                         None if c_p is None else c_p.data_ptr(),
+                         PI_ROWS_FP8_E4M3 if rows == "fp8" else PI_ROWS_FP16)
 
 
 class Layer:
     """A layer object of libpi (library-owned, permuted, neuron-major weights)."""
 
     def __init__(self, W_up, W_gate, b, W_down, W_p1, W_p2, c_p=None, act="relu",
-                 perm=None, stream=None):
-        desc = make_desc(W_up, W_gate, b, W_down, W_p1, W_p2, c_p, act)
+                 perm=None, stream=None, rows="fp16"):
+        desc = make_desc(W_up, W_gate, b, W_down, W_p1, W_p2, c_p, act, rows)
         self._h = C.c_void_p()
         perm_arr = None
         if perm is not None:
@@ -137,12 +143,13 @@ class Layer:
                                    _stream(stream)), "pi_layer_create")
         self.d, self.ffn, self.rank = int(desc.d), int(desc.ffn), int(desc.rank)
         self.act = "reglu" if desc.act == PI_ACT_REGLU else "relu"
+        self.rows = rows
         self.device = W_up.device
 
     @classmethod
-    def from_dict(cls, t: dict, perm=None, stream=None) -> "Layer":
+    def from_dict(cls, t: dict, perm=None, stream=None, rows="fp16") -> "Layer":
         return cls(t["W_up"], t.get("W_gate"), t["b"], t["W_down"], t["W_p1"], t["W_p2"],
-                   t.get("c_p"), t.get("act", "relu"), perm=perm, stream=stream)
+                   t.get("c_p"), t.get("act", "relu"), perm=perm, stream=stream, rows=rows)
 
     @property
     def handle(self) -> C.c_void_p:
@@ -159,6 +166,15 @@ class Layer:
                 lib.pi_layer_destroy(self._h)
         except Exception:
             pass
+
+    def rows_fp8(self, matrix: int, stream=None):
+        """Stored E4M3 codes (uint8 [ffn, d]) and row scales (fp32 [ffn]) of
+        matrix 0 (up), 1 (gate) or 2 (down^T), in storage order."""
+        codes = torch.empty(self.ffn, self.d, dtype=torch.uint8, device=self.device)
+        scales = torch.empty(self.ffn, dtype=torch.float32, device=self.device)
+        _check(lib.pi_layer_rows_fp8(self._h, int(matrix), _ptr(codes), _ptr(scales), _stream(stream)),
+               "pi_layer_rows_fp8")
+        return codes, scales
 
     def perm(self) -> np.ndarray:
         out = np.empty(self.ffn, dtype=np.int32)

@@ -36,6 +36,30 @@ __global__ void k_permute_rows(const __half *__restrict__ src, __half *__restric
 }
 
 // dst[k] = src ? src[perm[k]] : 0
+// Per-row E4M3 quantisation of W [rows, d] fp16 (the format of
+// PI_ROWS_FP8_E4M3): s = max |w| / 448 (1 for an all-zero row), codes of
+// w / s rounded to nearest even and saturated, both in binary32.
+__global__ void __launch_bounds__(256) k_quantize_rows(const __half *__restrict__ W, uint8_t *__restrict__ Q,
+                                                       float *__restrict__ scale, int rows, int d) {
+  __shared__ float red[8];
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const __half *w = W + (size_t)r * d;
+    float m = 0.f;
+    for (int j = threadIdx.x; j < d; j += blockDim.x) m = fmaxf(m, fabsf(__half2float(w[j])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+    for (int k = 1; k < (int)(blockDim.x >> 5); ++k) m = fmaxf(m, red[k]);
+    const float s = m > 0.f ? m / 448.0f : 1.0f;
+    for (int j = threadIdx.x; j < d; j += blockDim.x)
+      Q[(size_t)r * d + j] = __nv_cvt_float_to_fp8(__half2float(w[j]) / s, __NV_SATFINITE, __NV_E4M3);
+    if (threadIdx.x == 0) scale[r] = s;
+    __syncthreads();                  // red[] is reused by the next row
+  }
+}
+
 __global__ void k_permute_vec(const float *__restrict__ src, float *__restrict__ dst,
                               const int32_t *__restrict__ perm, int n) {
   for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += gridDim.x * blockDim.x)
@@ -129,6 +153,9 @@ pi_status check_desc(const pi_layer_desc *D) {
     return pi::fail(PI_ERR_INVALID_ARG, "a required weight pointer is NULL");
   if ((D->act == PI_ACT_REGLU) != (D->W_gate != nullptr))
     return pi::fail(PI_ERR_INVALID_ARG, "W_gate must be given exactly when act is PI_ACT_REGLU");
+  if (D->row_format != PI_ROWS_FP16 && D->row_format != PI_ROWS_FP8_E4M3)
+    return pi::fail(PI_ERR_INVALID_ARG, "row_format %d is neither PI_ROWS_FP16 nor PI_ROWS_FP8_E4M3",
+                    D->row_format);
   const void *h16[] = {D->W_up, D->W_gate, D->W_down, D->W_p1, D->W_p2};
   for (const void *p : h16)
     if (p && !aligned16(p)) return pi::fail(PI_ERR_INVALID_ARG, "fp16 weights must be 16-byte aligned");
@@ -255,6 +282,8 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   pi_layer *L = new (std::nothrow) pi_layer();
   if (!L) return pi::fail(PI_ERR_OOM, "host allocation failed");
   L->d = d; L->ffn = ffn; L->rank = r; L->act = D->act;
+  L->row_format = D->row_format;
+  const bool q8 = D->row_format == PI_ROWS_FP8_E4M3;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto bail = [&](pi_status code) {
     if (L->base) cudaFree(L->base);
@@ -281,9 +310,15 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   size_t off = 0;
   const size_t o_p1 = off; off += align_up((size_t)r * d * sizeof(__half));
   const size_t o_p2 = off; off += align_up((size_t)ffn * r * sizeof(__half));
-  const size_t o_up = off; off += align_up(wrow);
-  const size_t o_gate = off; if (D->act == PI_ACT_REGLU) off += align_up(wrow);
-  const size_t o_dT = off; off += align_up(wrow);
+  // the gathered rows: fp16, or E4M3 codes (1 byte) plus one scale per row
+  const size_t rowmat = q8 ? (size_t)ffn * d : wrow;
+  const size_t o_up = off; off += align_up(rowmat);
+  const size_t o_gate = off; if (D->act == PI_ACT_REGLU) off += align_up(rowmat);
+  const size_t o_dT = off; off += align_up(rowmat);
+  const size_t vsc = q8 ? align_up((size_t)ffn * sizeof(float)) : 0;
+  const size_t o_sup = off; off += vsc;
+  const size_t o_sgate = off; if (D->act == PI_ACT_REGLU) off += vsc;
+  const size_t o_sdT = off; off += vsc;
   const size_t o_b = off; off += align_up((size_t)ffn * sizeof(float));
   const size_t o_c = off; off += align_up((size_t)ffn * sizeof(float));
   const size_t o_perm = off; off += align_up((size_t)ffn * sizeof(int32_t));
@@ -302,9 +337,18 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   char *b = L->base;
   L->W_p1 = reinterpret_cast<__half *>(b + o_p1);
   L->W_p2 = reinterpret_cast<__half *>(b + o_p2);
-  L->W_up = reinterpret_cast<__half *>(b + o_up);
-  L->W_gate = D->act == PI_ACT_REGLU ? reinterpret_cast<__half *>(b + o_gate) : nullptr;
-  L->W_dT = reinterpret_cast<__half *>(b + o_dT);
+  if (!q8) {
+    L->W_up = reinterpret_cast<__half *>(b + o_up);
+    L->W_gate = D->act == PI_ACT_REGLU ? reinterpret_cast<__half *>(b + o_gate) : nullptr;
+    L->W_dT = reinterpret_cast<__half *>(b + o_dT);
+  } else {
+    L->Q_up = reinterpret_cast<uint8_t *>(b + o_up);
+    L->Q_gate = D->act == PI_ACT_REGLU ? reinterpret_cast<uint8_t *>(b + o_gate) : nullptr;
+    L->Q_dT = reinterpret_cast<uint8_t *>(b + o_dT);
+    L->s_up = reinterpret_cast<float *>(b + o_sup);
+    L->s_gate = D->act == PI_ACT_REGLU ? reinterpret_cast<float *>(b + o_sgate) : nullptr;
+    L->s_dT = reinterpret_cast<float *>(b + o_sdT);
+  }
   L->b = reinterpret_cast<float *>(b + o_b);
   L->c_p = reinterpret_cast<float *>(b + o_c);
   int32_t *perm_dev = reinterpret_cast<int32_t *>(b + o_perm);
@@ -324,17 +368,42 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   const int grid_rows = std::min(ffn, 65535);
   k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_p2), L->W_p2,
                                            perm_dev, ffn, r);
-  k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_up), L->W_up,
+  // FP8 layers: each permuted fp16 matrix goes through one temporary buffer
+  // and is quantised row by row into the layer
+  __half *tmp = nullptr;
+  if (q8) {
+    e = cudaMalloc(reinterpret_cast<void **>(&tmp), wrow);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return bail(pi::cuda_fail(e, "cudaMalloc(quantisation buffer)"));
+    }
+  }
+  auto fail_tmp = [&](cudaError_t e_, const char *what) {
+    if (tmp) {
+      cudaStreamSynchronize(s);
+      cudaFree(tmp);
+    }
+    return bail(pi::cuda_fail(e_, what));
+  };
+  const int grid_q = std::min(ffn, 4 * L->num_sms * 8);
+  k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_up), q8 ? tmp : L->W_up,
                                            perm_dev, ffn, d);
-  if (L->W_gate)
-    k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_gate),
-                                             L->W_gate, perm_dev, ffn, d);
+  if (q8) k_quantize_rows<<<grid_q, 256, 0, s>>>(tmp, L->Q_up, L->s_up, ffn, d);
+  if (D->act == PI_ACT_REGLU) {
+    k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_gate), q8 ? tmp : L->W_gate,
+                                             perm_dev, ffn, d);
+    if (q8) k_quantize_rows<<<grid_q, 256, 0, s>>>(tmp, L->Q_gate, L->s_gate, ffn, d);
+  }
   k_permute_vec<<<(ffn + 255) / 256, 256, 0, s>>>(D->b, L->b, perm_dev, ffn);
   k_permute_vec<<<(ffn + 255) / 256, 256, 0, s>>>(D->c_p, L->c_p, perm_dev, ffn);
   k_transpose_perm<<<dim3((ffn + 31) / 32, (d + 31) / 32), dim3(32, 8), 0, s>>>(
-      reinterpret_cast<const __half *>(D->W_down), L->W_dT, perm_dev, d, ffn);
-  PI_CREATE_CUDA(cudaGetLastError());
-  PI_CREATE_CUDA(cudaStreamSynchronize(s));
+      reinterpret_cast<const __half *>(D->W_down), q8 ? tmp : L->W_dT, perm_dev, d, ffn);
+  if (q8) k_quantize_rows<<<grid_q, 256, 0, s>>>(tmp, L->Q_dT, L->s_dT, ffn, d);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_tmp(e, "layer copy kernels");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_tmp(e, "cudaStreamSynchronize(create)");
+  if (tmp) cudaFree(tmp);
 #undef PI_CREATE_CUDA
   *out = L;
   return PI_OK;
@@ -357,6 +426,21 @@ pi_status pi_layer_info(const pi_layer *L, int32_t *d, int32_t *ffn, int32_t *ra
   if (ffn) *ffn = L->ffn;
   if (rank) *rank = L->rank;
   if (act) *act = L->act;
+  return PI_OK;
+}
+
+pi_status pi_layer_rows_fp8(const pi_layer *L, int32_t matrix, uint8_t *codes, float *scales,
+                            void *stream) {
+  g_err[0] = 0;
+  if (!L) return pi::fail(PI_ERR_INVALID_ARG, "layer is NULL");
+  if (L->row_format != PI_ROWS_FP8_E4M3) return pi::fail(PI_ERR_UNSUPPORTED, "the layer stores fp16 rows");
+  if (!codes || !scales) return pi::fail(PI_ERR_INVALID_ARG, "codes and scales must be non-NULL");
+  const uint8_t *q = matrix == 0 ? L->Q_up : matrix == 1 ? L->Q_gate : matrix == 2 ? L->Q_dT : nullptr;
+  const float *sc = matrix == 0 ? L->s_up : matrix == 1 ? L->s_gate : matrix == 2 ? L->s_dT : nullptr;
+  if (!q || !sc) return pi::fail(PI_ERR_INVALID_ARG, "matrix %d: need 0 (up), 1 (gate, ReGLU) or 2 (down)", matrix);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PI_TRY_CUDA(cudaMemcpyAsync(codes, q, (size_t)L->ffn * L->d, cudaMemcpyDeviceToDevice, s));
+  PI_TRY_CUDA(cudaMemcpyAsync(scales, sc, sizeof(float) * (size_t)L->ffn, cudaMemcpyDeviceToDevice, s));
   return PI_OK;
 }
 
@@ -383,6 +467,14 @@ static pi_status check_common(const pi_layer *L, const uint16_t *x, int32_t B, c
   if (ws_bytes < w->total)
     return pi::fail(PI_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu for B=%d", ws_bytes,
                     w->total, B);
+  return PI_OK;
+}
+
+// Entry points that read fp16 rows (the standalone sparse operators and the
+// tensor-core path) do not take FP8 layers.
+static pi_status need_fp16_rows(const pi_layer *L, const char *what) {
+  if (L->row_format != PI_ROWS_FP16)
+    return pi::fail(PI_ERR_UNSUPPORTED, "%s needs a layer with fp16 rows (this one stores FP8 E4M3 rows)", what);
   return PI_OK;
 }
 
@@ -421,6 +513,8 @@ pi_status pi_sparse_ffn(pi_layer *L, const uint16_t *x, int32_t B, const int32_t
   if (!idx || !count || !aligned4(idx) || !aligned4(count))
     return pi::fail(PI_ERR_INVALID_ARG, "idx and count must be non-NULL and 4-byte aligned");
   if (!y || !aligned16(y)) return pi::fail(PI_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
+  st = need_fp16_rows(L, "pi_sparse_ffn");
+  if (st != PI_OK) return st;
   PI_TRY_CUDA(pi::run_sparse_ffn(L, reinterpret_cast<const __half *>(x), B, idx, count, 0, y, w,
                                  static_cast<char *>(ws), static_cast<cudaStream_t>(stream)));
   return PI_OK;
@@ -433,6 +527,8 @@ pi_status pi_ffn_dense_ref(pi_layer *L, const uint16_t *x, int32_t B, float *y, 
   pi_status st = check_common(L, x, B, ws, ws_bytes, &w);
   if (st != PI_OK) return st;
   if (!y || !aligned16(y)) return pi::fail(PI_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
+  st = need_fp16_rows(L, "pi_ffn_dense_ref");
+  if (st != PI_OK) return st;
   PI_TRY_CUDA(pi::run_sparse_ffn(L, reinterpret_cast<const __half *>(x), B, nullptr, nullptr,
                                  L->ffn, y, w, static_cast<char *>(ws),
                                  static_cast<cudaStream_t>(stream)));
@@ -455,6 +551,8 @@ pi_status pi_layer_forward(pi_layer *L, const uint16_t *x, int32_t B, int32_t *i
     PI_TRY_CUDA(pi::run_stack(&L, 1, xh, B, idx, count, y, w, wsb, s));
     return PI_OK;
   }
+  st = need_fp16_rows(L, "pi_layer_forward with more than 2 tokens");
+  if (st != PI_OK) return st;
   uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
   if (pi::tc_predict_supported(L, B)) {
     PI_TRY_CUDA(pi::run_predict_tc(L, xh, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
@@ -477,8 +575,9 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
     const pi_layer *Ll = layers[l];
     if (!Ll) return pi::fail(PI_ERR_INVALID_ARG, "layers[%d] is NULL", l);
     if (Ll->d != layers[0]->d || Ll->ffn != layers[0]->ffn || Ll->rank != layers[0]->rank ||
-        Ll->act != layers[0]->act || Ll->device != layers[0]->device)
-      return pi::fail(PI_ERR_INVALID_ARG, "layers[%d] differs in shape, activation or device", l);
+        Ll->act != layers[0]->act || Ll->device != layers[0]->device ||
+        Ll->row_format != layers[0]->row_format)
+      return pi::fail(PI_ERR_INVALID_ARG, "layers[%d] differs in shape, activation, row format or device", l);
   }
   pi_layer *L = layers[0];
   pi::WsLayout w;
@@ -501,7 +600,9 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
                                 count ? count + l0 : nullptr, y + l0 * xs, w, wsb, s));
     }
     return PI_OK;
-  }
+  }  st = need_fp16_rows(L, "pi_stack_forward with more than 2 tokens");
+  if (st != PI_OK) return st;
+
   for (int l = 0; l < n_layers; ++l) {
     pi_layer *Ll = layers[l];
     uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -24,6 +25,11 @@ struct pi_layer {
   __half *W_up = nullptr;        // [ffn, d]      permuted rows
   __half *W_gate = nullptr;      // [ffn, d]      permuted rows (ReGLU)
   __half *W_dT = nullptr;        // [ffn, d]      W_down^T, permuted rows
+  // PI_ROWS_FP8_E4M3 layers keep the rows as E4M3 codes with a per-row scale
+  // instead (the fp16 row pointers above are then NULL)
+  int row_format = PI_ROWS_FP16;
+  uint8_t *Q_up = nullptr, *Q_gate = nullptr, *Q_dT = nullptr;   // [ffn, d]
+  float *s_up = nullptr, *s_gate = nullptr, *s_dT = nullptr;     // [ffn]
   float *b = nullptr;            // [ffn]         permuted
   float *c_p = nullptr;          // [ffn]         permuted (zeros when absent)
   unsigned int *status = nullptr;
@@ -63,12 +69,14 @@ struct WsLayout {
 };
 
 // Layers per persistent launch (longer stacks are split into several launches).
-constexpr int kMaxStack = 64;
+constexpr int kMaxStack = 32;
 
 
 // Device pointers of one layer, as the persistent kernel sees them.
 struct LayerDev {
-  const __half *W_p1, *W_p2, *W_up, *W_gate, *W_dT;
+  const __half *W_p1, *W_p2;
+  const void *R_up, *R_gate, *R_dT;   // rows: fp16, or E4M3 codes (FP8 layers)
+  const float *s_up, *s_gate, *s_dT;  // per-row scales (FP8 layers)
   const float *b, *c_p;
   int hot_per_slice;     // leading slice positions whose rows are fetched speculatively
 };
@@ -79,6 +87,7 @@ struct StackParams {
   int G, staged, lanes_l, pf_rows, pf_next;
   int off_flag, off_list, off_lb, off_a, off_stage, stage_bytes, slice_pad;   // shared memory layout
   int soff_c, soff_b, soff_p1, soff_p2;                     // offsets inside a stage buffer
+  int soff_su, soff_sg, soff_sd;                            // row-scale slices (FP8 layers)
   const __half *x;       // [n_layers, B, d]
   float *y;              // [n_layers, B, d]
   int32_t *count;        // [n_layers] or nullptr
@@ -204,6 +213,39 @@ __device__ __forceinline__ void axpy8(float *acc, float s, const uint4 &w) {
     acc[2 * e] = fmaf(s, wf.x, acc[2 * e]);
     acc[2 * e + 1] = fmaf(s, wf.y, acc[2 * e + 1]);
   }
+}
+
+// The same for 8 E4M3 codes (w) against 8 halves (x); E4M3 values are exact
+// in fp16 and the products exact in fp32.
+__device__ __forceinline__ float dot8_e4m3(float acc, const uint2 &w, const uint4 &x) {
+  const __nv_fp8x2_storage_t *wq = reinterpret_cast<const __nv_fp8x2_storage_t *>(&w);
+  const __half2 *xh = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(wq[e], __NV_E4M3);
+    float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+    float2 xf = __half22float2(xh[e]);
+    acc = fmaf(wf.x, xf.x, acc);
+    acc = fmaf(wf.y, xf.y, acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ void axpy8_e4m3(float *acc, float s, const uint2 &w) {
+  const __nv_fp8x2_storage_t *wq = reinterpret_cast<const __nv_fp8x2_storage_t *>(&w);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(wq[e], __NV_E4M3);
+    float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+    acc[2 * e] = fmaf(s, wf.x, acc[2 * e]);
+    acc[2 * e + 1] = fmaf(s, wf.y, acc[2 * e + 1]);
+  }
+}
+
+__device__ __forceinline__ uint2 ld_stream2(const uint2 *p) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -50,6 +50,8 @@ extern "C" pi_status pi_sparse_ffn_noalloc(pi_layer *L, const uint16_t *x, int32
                                            const int32_t *idx, const int32_t *count, float *y,
                                            void *stream) {
   if (!L) return pi::fail(PI_ERR_INVALID_ARG, "layer is NULL");
+  if (L->row_format != PI_ROWS_FP16)
+    return pi::fail(PI_ERR_UNSUPPORTED, "pi_sparse_ffn_noalloc needs a layer with fp16 rows");
   if (B < 1 || B > 2)
     return pi::fail(PI_ERR_UNSUPPORTED, "pi_sparse_ffn_noalloc handles batches of 1 or 2 tokens, got %d", B);
   if (!x || (reinterpret_cast<uintptr_t>(x) & 15u))

@@ -25,6 +25,8 @@
 // sets a status bit and returns (no trap, no unbounded wait).  Data written
 // inside the kernel (h, counts, partials) is read with ld.global.cg (L2,
 // coherent); only weights and x use the read-only path.
+#include <type_traits>
+
 #include "pi_internal.cuh"
 
 namespace {
@@ -136,7 +138,10 @@ __device__ unsigned long long g_cta_e[160][16][2];
 __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half *x, int nb, int cta,
                                             int G, int d, int r, int s0, int s1, bool with_pred,
                                             __half *x_s, float *c_s, float *b_s, __half *p1_s,
-                                            __half *p2_s, uint32_t mbar) {
+                                            __half *p2_s, float *su_s, float *sg_s, float *sd_s,
+                                            uint32_t mbar) {
+  // su_s / sg_s / sd_s: the row-scale slices of an FP8 layer (up, gate for
+  // ReGLU, down^T), or nullptr
   const int s0a = s0 & ~3;
   const uint32_t cb_bytes = (uint32_t)(((s1 - s0a) + 3) & ~3) * 4u;
   const uint32_t x_bytes = (uint32_t)nb * (uint32_t)d * 2u;
@@ -145,12 +150,18 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
   int na = 0;
   if (with_pred)
     for (int k = cta; k < r; k += G) ++na;
-  const uint32_t total = x_bytes + (cb_bytes ? 2u * cb_bytes : 0u) + (uint32_t)na * row_bytes + p2_bytes;
+  const uint32_t nsc = su_s ? (sg_s ? 3u : 2u) : 0u;
+  const uint32_t total = x_bytes + (cb_bytes ? (2u + nsc) * cb_bytes : 0u) + (uint32_t)na * row_bytes + p2_bytes;
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(total) : "memory");
   tma_load_1d(x_s, x, x_bytes, mbar);
   if (cb_bytes) {
     tma_load_1d(c_s, Ld.c_p + s0a, cb_bytes, mbar);
     tma_load_1d(b_s, Ld.b + s0a, cb_bytes, mbar);
+    if (su_s) {
+      tma_load_1d(su_s, Ld.s_up + s0a, cb_bytes, mbar);
+      if (sg_s) tma_load_1d(sg_s, Ld.s_gate + s0a, cb_bytes, mbar);
+      tma_load_1d(sd_s, Ld.s_dT + s0a, cb_bytes, mbar);
+    }
   }
   int q = 0;
   for (int k = cta; q < na; k += G, ++q)
@@ -158,8 +169,12 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
   if (p2_bytes) tma_load_1d(p2_s, Ld.W_p2 + (size_t)s0 * r, p2_bytes, mbar);
 }
 
-template <int CPT, int NB, bool REGLU>
+template <int CPT, int NB, bool REGLU, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constant__ pi::StackParams p) {
+  // FP8: the up / gate / down rows are E4M3 codes (8 bytes per 8 elements,
+  // loaded as uint2) with a per-row scale applied to each dot product and
+  // activation; otherwise fp16 (uint4 per 8 elements)
+  using RowVec = typename std::conditional<FP8, uint2, uint4>::type;
   constexpr int NR = REGLU ? 2 : 1;                          // gated rows per neuron
   constexpr int LOADS = CPT == 1 ? 24 : 16;                  // 16-byte loads in flight per thread
   constexpr int GU0 = LOADS / (CPT * NR), GD0 = LOADS / CPT;
@@ -175,8 +190,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
   const int d = p.d, ffn = p.ffn, r = p.rank, nv = d >> 3;
-  const uint32_t row_bytes = (uint32_t)d * 2u;
+  const uint32_t row_bytes = (uint32_t)d * 2u;                 // an fp16 row (predictor)
+  const uint32_t rrow = FP8 ? (uint32_t)d : row_bytes;          // a gathered up / gate / down row
   unsigned *status = p.status;
+  // 8-element vector v of gathered row i of R (fp16 or E4M3 codes)
+  auto ldrow = [&](const void *R, int i, int v) -> RowVec {
+    const char *row = static_cast<const char *>(R) + (size_t)i * rrow;
+    if constexpr (FP8) return pidev::ld_stream2(reinterpret_cast<const uint2 *>(row) + v);
+    else return pidev::ld_stream(reinterpret_cast<const uint4 *>(row) + v);
+  };
+  auto rowdot = [](float acc, const RowVec &w, const uint4 &x) {
+    if constexpr (FP8) return pidev::dot8_e4m3(acc, w, x);
+    else return pidev::dot8(acc, w, x);
+  };
+  auto rowaxpy = [](float *acc, float a, const RowVec &w) {
+    if constexpr (FP8) pidev::axpy8_e4m3(acc, a, w);
+    else pidev::axpy8(acc, a, w);
+  };
+  auto rowpf = [&](const void *R, int i) {
+    pidev::prefetch_l2_bulk(static_cast<const char *>(R) + (size_t)i * rrow, rrow);
+  };
   unsigned epoch = 0;
   const uint32_t mbar0 = smem_u32(&mbar_s[0]);
 
@@ -200,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     stage_layer(p.layers[layer], p.x + (size_t)layer * NB * d, NB, cta, G, d, r, s0, s1,
                 p.staged != 0, reinterpret_cast<__half *>(bsm), reinterpret_cast<float *>(bsm + p.soff_c),
                 reinterpret_cast<float *>(bsm + p.soff_b), reinterpret_cast<__half *>(bsm + p.soff_p1),
-                reinterpret_cast<__half *>(bsm + p.soff_p2), mbar0 + 8u * (uint32_t)(layer & 1));
+                reinterpret_cast<__half *>(bsm + p.soff_p2),
+                FP8 ? reinterpret_cast<float *>(bsm + p.soff_su) : nullptr,
+                FP8 && REGLU ? reinterpret_cast<float *>(bsm + p.soff_sg) : nullptr,
+                FP8 ? reinterpret_cast<float *>(bsm + p.soff_sd) : nullptr, mbar0 + 8u * (uint32_t)(layer & 1));
   };
 
   if (tid == 0) {
@@ -229,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     const __half *x_s = reinterpret_cast<const __half *>(bsm);
     const float *c_s = reinterpret_cast<const float *>(bsm + p.soff_c);
     const float *b_s = reinterpret_cast<const float *>(bsm + p.soff_b);
+    // FP8 layers: row scales of the slice (up, gate for ReGLU, down^T)
+    const float *sc_up = reinterpret_cast<const float *>(bsm + p.soff_su);
+    const float *sc_gate = reinterpret_cast<const float *>(bsm + p.soff_sg);
+    const float *sc_dn = reinterpret_cast<const float *>(bsm + p.soff_sd);
     const __half *p1_s = reinterpret_cast<const __half *>(bsm + p.soff_p1);
     const __half *p2_s = reinterpret_cast<const __half *>(bsm + p.soff_p2);
     uint4 xr[NB][CPT];
@@ -296,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     // before it slowed the barrier itself.)
     if (tid >= kIssuer && tid < kIssuer + n_hot) {
       const int i = s0 + tid - kIssuer;
-      pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
-      if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
-      pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+      rowpf(Ld.R_up, i);
+      if (REGLU) rowpf(Ld.R_gate, i);
+      rowpf(Ld.R_dT, i);
     }
     for (int e = tid; e < NB * r; e += kThreads) h_s[e] = ldcg(p.h + e);
     __syncthreads();
@@ -440,9 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         for (int j = tid - kIssuer; j < npf; j += 32) {
           const int i = list_s[j];
           if (i - s0 < n_hot) continue;        // requested after the first barrier
-          pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
-          if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
-          pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+          rowpf(Ld.R_up, i);
+          if (REGLU) rowpf(Ld.R_gate, i);
+          rowpf(Ld.R_dT, i);
         }
       for (int j = tid; j < lcount; j += kThreads) lb_s[j] = b_s[list_s[j] - s0a];
       if (p.mask_out)
@@ -477,13 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     if (lcount > p.pf_rows)                     // rows past the early-prefetch budget
       for (int j = p.pf_rows + tid; j < lcount; j += kThreads) {
         const int i = list_s[j];
-        pidev::prefetch_l2_bulk(Ld.W_up + (size_t)i * d, row_bytes);
-        if (REGLU) pidev::prefetch_l2_bulk(Ld.W_gate + (size_t)i * d, row_bytes);
-        pidev::prefetch_l2_bulk(Ld.W_dT + (size_t)i * d, row_bytes);
+        rowpf(Ld.R_up, i);
+        if (REGLU) rowpf(Ld.R_gate, i);
+        rowpf(Ld.R_dT, i);
       }
     for (int w0 = 0; w0 < lcount; w0 += GU) {
       const int n_here = min(GU, lcount - w0);
-      uint4 wu[GU][NR][CPT];
+      RowVec wu[GU][NR][CPT];
 #pragma unroll
       for (int n = 0; n < GU; ++n) {
         const int i = n < n_here ? list_s[w0 + n] : -1;
@@ -491,11 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         for (int c = 0; c < CPT; ++c) {
           const int v = tid + c * kThreads;
           const bool ok = i >= 0 && v < nv;
-          wu[n][0][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_up + (size_t)i * d) + v)
-                           : make_uint4(0, 0, 0, 0);
-          if (REGLU)
-            wu[n][NR - 1][c] = ok ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_gate + (size_t)i * d) + v)
-                                  : make_uint4(0, 0, 0, 0);
+          wu[n][0][c] = ok ? ldrow(Ld.R_up, i, v) : RowVec{};
+          if (REGLU) wu[n][NR - 1][c] = ok ? ldrow(Ld.R_gate, i, v) : RowVec{};
         }
       }
 #pragma unroll
@@ -506,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           for (int t = 0; t < NB; ++t) {
             float sdot = 0.f;
 #pragma unroll
-            for (int c = 0; c < CPT; ++c) sdot = pidev::dot8(sdot, wu[n][q][c], xr[t][c]);
+            for (int c = 0; c < CPT; ++c) sdot = rowdot(sdot, wu[n][q][c], xr[t][c]);
             sdot = pidev::warp_sum(sdot);
             if (lane == 0) red_s[wid][t][q][n] = sdot;
           }
@@ -519,6 +556,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           for (int q = 0; q < kWarps; ++q) {   // fixed order over warps
             su += red_s[q][t][0][n];
             if (REGLU) sg += red_s[q][t][NR - 1][n];
+          }
+          if (FP8) {                           // row scales (staged slices)
+            const int k = list_s[w0 + n] - s0a;
+            su *= sc_up[k];
+            if (REGLU) sg *= sc_gate[k];
           }
           float a;
           if (REGLU) {
@@ -535,16 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     }
     for (int w0 = 0; w0 < lcount; w0 += GD) {
       const int n_here = min(GD, lcount - w0);
-      uint4 wd[GD][CPT];
+      RowVec wd[GD][CPT];
 #pragma unroll
       for (int n = 0; n < GD; ++n) {
         const int i = n < n_here ? list_s[w0 + n] : -1;
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
           const int v = tid + c * kThreads;
-          wd[n][c] = (i >= 0 && v < nv)
-                         ? pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_dT + (size_t)i * d) + v)
-                         : make_uint4(0, 0, 0, 0);
+          wd[n][c] = (i >= 0 && v < nv) ? ldrow(Ld.R_dT, i, v) : RowVec{};
         }
       }
 #pragma unroll
@@ -552,9 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         if (n < n_here) {
 #pragma unroll
           for (int t = 0; t < NB; ++t) {
-            const float an = a_all[t * p.slice_pad + w0 + n];
+            float an = a_all[t * p.slice_pad + w0 + n];
+            if (FP8) an *= sc_dn[list_s[w0 + n] - s0a];
 #pragma unroll
-            for (int c = 0; c < CPT; ++c) pidev::axpy8(acc[t][c], an, wd[n][c]);
+            for (int c = 0; c < CPT; ++c) rowaxpy(acc[t][c], an, wd[n][c]);
           }
         }
       }
@@ -648,9 +689,9 @@ extern "C" int pi_debug_cta_e(unsigned long long *out) {
 namespace {
 #endif
 
-template <int CPT, int NB, bool REGLU>
+template <int CPT, int NB, bool REGLU, bool FP8>
 cudaError_t launch_step(const pi::StackParams &p, size_t smem, cudaStream_t s) {
-  auto kern = k_stack_step<CPT, NB, REGLU>;
+  auto kern = k_stack_step<CPT, NB, REGLU, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 0;
@@ -670,14 +711,14 @@ cudaError_t launch_step(const pi::StackParams &p, size_t smem, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int NB, bool REGLU>
+template <int NB, bool REGLU, bool FP8>
 cudaError_t dispatch_step(const pi::StackParams &p, size_t smem, cudaStream_t s) {
   const int cpt = (p.d / 8 + kThreads - 1) / kThreads;
   switch (cpt) {
-    case 1: return launch_step<1, NB, REGLU>(p, smem, s);
-    case 2: return launch_step<2, NB, REGLU>(p, smem, s);
-    case 3: return launch_step<3, NB, REGLU>(p, smem, s);
-    case 4: return launch_step<4, NB, REGLU>(p, smem, s);
+    case 1: return launch_step<1, NB, REGLU, FP8>(p, smem, s);
+    case 2: return launch_step<2, NB, REGLU, FP8>(p, smem, s);
+    case 3: return launch_step<3, NB, REGLU, FP8>(p, smem, s);
+    case 4: return launch_step<4, NB, REGLU, FP8>(p, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -690,6 +731,7 @@ size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 struct SmemPlan {
   size_t off_flag, off_list, off_lb, off_a, off_stage;   // absolute offsets
   size_t soff_c, soff_b, soff_p1, soff_p2;              // offsets inside a stage buffer
+  size_t soff_su, soff_sg, soff_sd;                      // FP8 row-scale slices (empty for fp16)
   size_t stage_small, stage_full;                        // buffer size without / with predictor
   size_t base_end;
 };
@@ -709,6 +751,11 @@ SmemPlan smem_plan(const pi_layer *L, int B) {
   size_t so = align128(2 * (size_t)B * L->d);                     // x
   s.soff_c = so;     so = align128(so + sizeof(float) * (slice + 8));
   s.soff_b = so;     so = align128(so + sizeof(float) * (slice + 8));
+  const bool q8 = L->row_format == PI_ROWS_FP8_E4M3;
+  const size_t sc = q8 ? sizeof(float) * (slice + 8) : 0;
+  s.soff_su = so;    so = align128(so + sc);
+  s.soff_sg = so;    so = align128(so + (L->act == PI_ACT_REGLU ? sc : 0));
+  s.soff_sd = so;    so = align128(so + sc);
   s.stage_small = so;
   s.soff_p1 = so;    so = align128(so + na_max * L->d * 2);
   s.soff_p2 = so;    so = align128(so + slice * L->rank * 2);
@@ -756,12 +803,16 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   p.soff_b = (int)sp.soff_b;
   p.soff_p1 = (int)sp.soff_p1;
   p.soff_p2 = (int)sp.soff_p2;
+  p.soff_su = (int)sp.soff_su;
+  p.soff_sg = (int)sp.soff_sg;
+  p.soff_sd = (int)sp.soff_sd;
   int GL = 32;
   while (GL > 8 && GL * 8 > L0->rank) GL >>= 1;
   p.lanes_l = GL;
   const int rows_per_neuron = L0->act == PI_ACT_REGLU ? 3 : 2;
   // early L2 prefetch of the local active rows: up to ~768 KB of rows per CTA
-  const int pf = (768 * 1024) / (2 * L0->d * rows_per_neuron);
+  const int rb = L0->row_format == PI_ROWS_FP8_E4M3 ? L0->d : 2 * L0->d;   // bytes of a gathered row
+  const int pf = (768 * 1024) / (rb * rows_per_neuron);
   p.pf_rows = pf < 1 ? 1 : pf;
   const size_t pred_bytes = 2ull * L0->rank * L0->d + 2ull * L0->ffn * L0->rank;
   p.pf_next = pred_bytes <= (32ull << 20);
@@ -779,18 +830,26 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
     // the k-th neuron of the caller's order sits at slice k % G, place k / G:
     // the first n_hot of them fill places 0 .. ceil(n_hot / G) - 1 of the slices
     const int hot = (Ll->n_hot + p.G - 1) / p.G;
-    p.layers[l] = LayerDev{Ll->W_p1, Ll->W_p2, Ll->W_up, Ll->W_gate, Ll->W_dT, Ll->b, Ll->c_p, hot};
+    const bool q8 = Ll->row_format == PI_ROWS_FP8_E4M3;
+    p.layers[l] = LayerDev{Ll->W_p1, Ll->W_p2,
+                           q8 ? static_cast<const void *>(Ll->Q_up) : Ll->W_up,
+                           q8 ? static_cast<const void *>(Ll->Q_gate) : Ll->W_gate,
+                           q8 ? static_cast<const void *>(Ll->Q_dT) : Ll->W_dT,
+                           Ll->s_up, Ll->s_gate, Ll->s_dT, Ll->b, Ll->c_p, hot};
   }
   cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
   const size_t smem = step_smem(L0, B);
   const bool reglu = L0->act == PI_ACT_REGLU;
+  const bool q8 = L0->row_format == PI_ROWS_FP8_E4M3;
   e = record_hook(L0->ev_before, s);
   if (e != cudaSuccess) return e;
   if (B == 1)
-    e = reglu ? dispatch_step<1, true>(p, smem, s) : dispatch_step<1, false>(p, smem, s);
+    e = q8 ? (reglu ? dispatch_step<1, true, true>(p, smem, s) : dispatch_step<1, false, true>(p, smem, s))
+           : (reglu ? dispatch_step<1, true, false>(p, smem, s) : dispatch_step<1, false, false>(p, smem, s));
   else
-    e = reglu ? dispatch_step<2, true>(p, smem, s) : dispatch_step<2, false>(p, smem, s);
+    e = q8 ? (reglu ? dispatch_step<2, true, true>(p, smem, s) : dispatch_step<2, false, true>(p, smem, s))
+           : (reglu ? dispatch_step<2, true, false>(p, smem, s) : dispatch_step<2, false, false>(p, smem, s));
   if (e != cudaSuccess) return e;
   e = record_hook(L0->ev_after, s);
   if (e != cudaSuccess) return e;

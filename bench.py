@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0, help="override tokens per step (debug)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rows", choices=["fp16", "fp8"], default="fp16",
+                    help="storage of the gathered up/gate/down rows (fp8: E4M3 codes, per-row scale)")
     ap.add_argument("--batch", type=int, default=1,
                     help="tokens per decode batch (the headline metric is batch 1)")
     return ap.parse_args()
@@ -62,10 +64,11 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def bytes_per_active_neuron(d: int, act: str) -> int:
+def bytes_per_active_neuron(d: int, act: str, rows: str = "fp16") -> int:
     """Weight bytes read per active neuron: its up row (+ gate row) and its
-    W_down^T row, 2d bytes each."""
-    return 2 * d * (3 if act == "reglu" else 2)
+    W_down^T row, 2d bytes each (fp8 rows: d code bytes + a 4-byte scale)."""
+    per_row = d + 4 if rows == "fp8" else 2 * d
+    return per_row * (3 if act == "reglu" else 2)
 
 
 def predictor_bytes(d: int, ffn: int, r: int) -> int:
@@ -129,7 +132,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
-def build_stack(cfg, device, n_layers, keep_host_layers):
+def build_stack(cfg, device, n_layers, keep_host_layers, rows="fp16"):
     import activation_sparse_rank_gb300 as pi
     spec = cfg.layer
     layers, host_layers = [], []
@@ -144,7 +147,7 @@ def build_stack(cfg, device, n_layers, keep_host_layers):
             # hot: active on more than half of the profiled tokens
             n_hot = int((counts > cfg.profile_tokens // 2).sum())
             del Xp
-        layer = pi.Layer.from_dict(t, perm=perm)
+        layer = pi.Layer.from_dict(t, perm=perm, rows=rows)
         layer.set_hot_count(n_hot)
         layers.append(layer)
         if l < keep_host_layers:
@@ -155,11 +158,12 @@ def build_stack(cfg, device, n_layers, keep_host_layers):
     return layers, host_layers
 
 
-def touched_bytes(cfg, counts: torch.Tensor) -> int:
+def touched_bytes(cfg, counts: torch.Tensor, rows: str = "fp16") -> int:
     spec = cfg.layer
     T, L = counts.shape
     s = int(counts.sum().item())
-    return T * L * predictor_bytes(spec.d, spec.ffn, spec.rank) + s * bytes_per_active_neuron(spec.d, spec.act)
+    return (T * L * predictor_bytes(spec.d, spec.ffn, spec.rank)
+            + s * bytes_per_active_neuron(spec.d, spec.act, rows))
 
 
 def time_oracle(host_layers, X_host, L_total, seconds: float, min_pairs: int = 4):
@@ -237,12 +241,13 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(cfg, n_layers: int, T: int, Bt: int, world: int) -> dict:
+def workload_config(cfg, n_layers: int, T: int, Bt: int, world: int, rows: str = "fp16") -> dict:
     """The config object both arms print for one workload."""
     spec = cfg.layer
+    weights = "fp16" if rows == "fp16" else "fp16 predictor; up/gate/down rows FP8 E4M3 with a per-row fp32 scale"
     return {"workload": cfg.description, "name": cfg.name, "d": spec.d, "ffn": spec.ffn,
             "rank": spec.rank, "layers": n_layers, "tokens_per_step": T * Bt, "batch": Bt,
-            "act": spec.act, "weights": "fp16", "hot_first": bool(cfg.profile_tokens),
+            "act": spec.act, "weights": weights, "hot_first": bool(cfg.profile_tokens),
             "l2": "inputs larger than L2: the distinct weight rows of a step exceed the 129 MB L2",
             "parallelism": f"replicas{world}"}
 
@@ -290,9 +295,14 @@ def main():
     n_layers = args.layers or cfg.layers
     T = args.tokens or cfg.tokens
     Bt = args.batch
-    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1 and Bt == 1
+    rows = args.rows
+    if rows == "fp8" and Bt > 2:
+        raise SystemExit("--rows fp8 runs at batch 1 or 2 (the persistent decode step)")
+    # the CPU baseline times the fp16 oracle; it belongs to the fp16 workload
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1 and Bt == 1 and rows == "fp16"
     t_setup = time.perf_counter()
-    layers, host_layers = build_stack(cfg, device, n_layers, keep_host_layers=2 if want_cpu else 0)
+    layers, host_layers = build_stack(cfg, device, n_layers, keep_host_layers=2 if want_cpu else 0,
+                                      rows=rows)
     stack = SparseFFNStack(layers, tokens=T, B=Bt)
     X = make_tokens(spec.d, T * n_layers * Bt, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
     stack.x.copy_(X.view(T, n_layers, Bt, spec.d))
@@ -331,37 +341,40 @@ def main():
 
     tokens_step = T * Bt
     value = tokens_step * world / (ms / 1000.0)
-    tb = touched_bytes(cfg, stack.count)
+    tb = touched_bytes(cfg, stack.count, rows)
     mean_S = float(stack.count.double().mean().item())
     eff_gbs = tb / (ms / 1000.0) / 1e9
     peak, peak_kind = measured_peaks()
     gpu_launches = stack.launches_per_step() * args.steps
 
-    # dense comparator: the same kernels over every neuron, 16 tokens
-    Td = min(16, T)
-    dense_g = torch.cuda.CUDAGraph()
-    ws = stack.ws
-    yd = torch.empty(n_layers, Bt, spec.d, dtype=torch.float32, device=device)
-    with torch.cuda.stream(s):
-        for li, layer in enumerate(layers):
-            layer.dense_ref(stack.x[0, li], yd[li], ws=ws, stream=s)
-    s.synchronize()
-    with torch.cuda.graph(dense_g, stream=s):
-        for t in range(Td):
+    # dense comparator: the same kernels over every neuron, 16 tokens (fp16
+    # rows only: the standalone operators read fp16 rows)
+    dense_tok_s = None
+    if rows == "fp16":
+        Td = min(16, T)
+        dense_g = torch.cuda.CUDAGraph()
+        ws = stack.ws
+        yd = torch.empty(n_layers, Bt, spec.d, dtype=torch.float32, device=device)
+        with torch.cuda.stream(s):
             for li, layer in enumerate(layers):
-                layer.dense_ref(stack.x[t, li], yd[li], ws=ws, stream=s)
-    for _ in range(2):
-        dense_g.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    with torch.cuda.stream(s):
-        for _ in range(3):
+                layer.dense_ref(stack.x[0, li], yd[li], ws=ws, stream=s)
+        s.synchronize()
+        with torch.cuda.graph(dense_g, stream=s):
+            for t in range(Td):
+                for li, layer in enumerate(layers):
+                    layer.dense_ref(stack.x[t, li], yd[li], ws=ws, stream=s)
+        for _ in range(2):
             dense_g.replay()
-    e1.record(s)
-    torch.cuda.synchronize()
-    dense_tok_s = 3 * Td * Bt / (e0.elapsed_time(e1) / 1000.0)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                dense_g.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        dense_tok_s = 3 * Td * Bt / (e0.elapsed_time(e1) / 1000.0)
 
     # dominant kernel (the persistent step kernel, one launch per token)
     # timed inside a captured step with external event-record nodes
@@ -395,7 +408,7 @@ def main():
     cnt = stack.count[:Tr].cpu().numpy()
     if Bt <= 2:   # the persistent step: predictor + rows of every layer
         alg_bytes = (Tr * n_layers * predictor_bytes(spec.d, spec.ffn, spec.rank)
-                     + float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act))
+                     + float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act, rows))
         kname = f"k_stack_step (one token through {n_layers} layers)"
     else:         # tensor-core up + down of layer 0: its active rows
         alg_bytes = float(cnt[:, 0].sum()) * bytes_per_active_neuron(spec.d, spec.act)
@@ -408,7 +421,7 @@ def main():
         tj = json.loads(tfile.read_text())
         if tj.get("kernel_source_hash") == kernel_source_hash():
             traffic = tj.get("bytes_per_launch")
-    if Bt > 2:
+    if Bt > 2 or rows != "fp16":     # the stored counters are of the fp16 step kernel
         traffic = None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
@@ -455,12 +468,13 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": workload_config(cfg, n_layers, T, Bt, world),
+            "config": workload_config(cfg, n_layers, T, Bt, world, rows),
             "effective_hbm_gbs": eff_gbs,
             "effective_frac_of_measured": eff_gbs / peak,
             "effective_frac_of_nominal_8tbs": eff_gbs / (NOMINAL_HBM_GBS),
             "touched_bytes_per_step": tb, "mean_active": mean_S,
-            "dense_tokens_per_s": dense_tok_s, "speedup_vs_dense": value / world / dense_tok_s,
+            "dense_tokens_per_s": dense_tok_s,
+            "speedup_vs_dense": value / world / dense_tok_s if dense_tok_s else None,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": gpu_launches, "clocks": clk, "setup_s": setup_s,
         }

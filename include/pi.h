@@ -50,6 +50,21 @@ typedef enum {
   PI_ACT_REGLU = 1   /* a_i = max(0, W_gate_i.x + b_i) * (W_up_i.x)            */
 } pi_act;
 
+/* Storage of the up / gate / down rows that the sparse operators gather.
+ * The report's results include quantised weights (section 3.1, Finding 2:
+ * INT4 runs); this library's quantised format is its own choice: FP8 E4M3
+ * codes with one fp32 scale per stored row, which halves the bytes a gathered
+ * row costs while the predictor stays fp16.
+ *   PI_ROWS_FP8_E4M3: for each row w of W_up, W_gate and W_down^T (d values):
+ *     s = max_j |w_j| / 448 in binary32 (s = 1 when the row is all zero),
+ *     q_j = the E4M3 code of w_j / s (binary32 division, round to nearest
+ *           even, saturating to +-448),
+ *   and the row stands for s * q_j.  The FFN is the FFN of these weights. */
+typedef enum {
+  PI_ROWS_FP16 = 0,
+  PI_ROWS_FP8_E4M3 = 1
+} pi_row_format;
+
 /* Shape limits (PI_ERR_UNSUPPORTED outside them). */
 #define PI_MAX_D      16384   /* d % 8 == 0 */
 #define PI_MAX_RANK   2048    /* rank % 8 == 0 */
@@ -66,7 +81,9 @@ typedef struct pi_layer pi_layer;
  *   W_down [d, ffn]   fp16  down projection
  *   W_p1   [rank, d]  fp16  predictor first layer (no bias)
  *   W_p2   [ffn, rank] fp16 predictor second layer
- *   c_p    [ffn]      fp32  predictor output bias, or NULL for zero */
+ *   c_p    [ffn]      fp32  predictor output bias, or NULL for zero
+ *   row_format        pi_row_format of the stored up / gate / down rows
+ *                     (0, PI_ROWS_FP16, keeps them as given) */
 typedef struct {
   int32_t d, ffn, rank;
   int32_t act;               /* pi_act */
@@ -77,6 +94,7 @@ typedef struct {
   const uint16_t *W_p1;
   const uint16_t *W_p2;
   const float *c_p;
+  int32_t row_format;        /* pi_row_format */
 } pi_layer_desc;
 
 /* Build a layer object that owns a permuted, neuron-major copy of the weights
@@ -95,8 +113,15 @@ typedef struct {
  * each neuron's down weights are one contiguous row.  Peak device memory is
  * the caller's weights plus one layer copy.  Synchronous: returns after the
  * copy finished on `stream`.  The caller may free its buffers afterwards.
- * Errors: PI_ERR_INVALID_ARG (NULL pointer, bad perm), PI_ERR_UNSUPPORTED
- * (shape), PI_ERR_OOM, PI_ERR_CUDA. *out is NULL on failure. */
+ * With row_format PI_ROWS_FP8_E4M3 the permuted up / gate / down^T rows are
+ * quantised on the device as described at pi_row_format and only the codes
+ * and scales are kept (d + 4 bytes per row); such a layer runs in
+ * pi_predict, pi_compact_active, and pi_layer_forward / pi_stack_forward for
+ * batches of 1 or 2 tokens; the other entry points return
+ * PI_ERR_UNSUPPORTED for it.
+ * Errors: PI_ERR_INVALID_ARG (NULL pointer, bad perm, unknown row_format),
+ * PI_ERR_UNSUPPORTED (shape), PI_ERR_OOM, PI_ERR_CUDA. *out is NULL on
+ * failure. */
 pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *desc,
                           const int32_t *perm, void *stream);
 
@@ -107,6 +132,14 @@ pi_status pi_layer_destroy(pi_layer *layer);
 /* Shape of a layer (any output pointer may be NULL). */
 pi_status pi_layer_info(const pi_layer *layer, int32_t *d, int32_t *ffn,
                         int32_t *rank, int32_t *act);
+
+/* Copy the stored FP8 rows of a PI_ROWS_FP8_E4M3 layer, in storage order:
+ *   matrix  0 W_up, 1 W_gate (ReGLU only), 2 W_down^T
+ *   codes   device uint8 [ffn, d] (E4M3 bit patterns)
+ *   scales  device fp32 [ffn]
+ * Asynchronous on `stream`.  PI_ERR_UNSUPPORTED for an fp16 layer. */
+pi_status pi_layer_rows_fp8(const pi_layer *layer, int32_t matrix, uint8_t *codes,
+                            float *scales, void *stream);
 
 /* Copy the layer's storage order (host int32 [ffn]): position k holds model
  * neuron perm[k].  Active-set indices returned by this library are positions
