@@ -180,8 +180,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   constexpr int GU0 = LOADS / (CPT * NR), GD0 = LOADS / CPT;
   constexpr int GU = GU0 > 0 ? GU0 : 1;                      // neurons per up-pass window
   constexpr int GD = GD0 > 0 ? GD0 : 1;                      // neurons per down-pass window
+  // one-pass windows: each neuron's up (+gate) and down rows loaded together,
+  // 96 registers of rows in flight per thread (56 with two tokens, whose
+  // inputs and accumulators take twice the registers)
+  constexpr int RV = FP8 ? 2 : 4;                            // 32-bit registers per row vector
+  constexpr int GW0 = (NB == 1 ? 96 : 56) / ((NR + 1) * CPT * RV);
+  constexpr int GW = GW0 > 0 ? GW0 : 1;                      // neurons per window
+  constexpr int GR = GU > GW ? GU : GW;
+  // Measured on GB300: the one-pass windows win with E4M3 rows (a window of
+  // 24 neurons covers nearly every CTA's list), with two tokens and with
+  // ReGLU (three rows per neuron); with one token of fp16 ReLU rows the two
+  // passes are as fast or slightly faster.
+  constexpr bool kOnePass = FP8 || NB == 2 || REGLU;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float red_s[kWarps][NB][NR][GU];
+  __shared__ float red_s[kWarps][NB][NR][GR];
   __shared__ float ared_s[kWarps][NB][8];
   __shared__ float4 fred_s[2][8];
   __shared__ int wtot_s[kWarps];
@@ -503,10 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     CTA_E_BEGIN(l);
 
     // ---------------- E: up (+gate) and down rows of my active neurons, in
-    // two passes: all up-row dot products first (a into shared memory), then
-    // all down rows.  The down rows were asked of L2 at the end of phase C,
-    // so they arrive while the up pass runs, and a CTA with many active
-    // neurons needs no extra round trip per extra window.
+    // windows of one pass or in two passes (kOnePass).
     float acc[NB][CPT][8];
 #pragma unroll
     for (int t = 0; t < NB; ++t)
@@ -521,6 +530,80 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         if (REGLU) rowpf(Ld.R_gate, i);
         rowpf(Ld.R_dT, i);
       }
+    if constexpr (kOnePass) {
+    // One pass of windows: a window's up (+gate) and down rows are requested
+    // together, so a window costs one memory round trip.
+    for (int w0 = 0; w0 < lcount; w0 += GW) {
+      const int n_here = min(GW, lcount - w0);
+      RowVec wu[GW][NR][CPT], wd[GW][CPT];
+#pragma unroll
+      for (int n = 0; n < GW; ++n) {
+        const int i = n < n_here ? list_s[w0 + n] : -1;
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          const int v = tid + c * kThreads;
+          const bool ok = i >= 0 && v < nv;
+          wu[n][0][c] = ok ? ldrow(Ld.R_up, i, v) : RowVec{};
+          if (REGLU) wu[n][NR - 1][c] = ok ? ldrow(Ld.R_gate, i, v) : RowVec{};
+          wd[n][c] = ok ? ldrow(Ld.R_dT, i, v) : RowVec{};
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < GW; ++n)
+#pragma unroll
+        for (int q = 0; q < NR; ++q)
+#pragma unroll
+          for (int t = 0; t < NB; ++t) {
+            float sdot = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) sdot = rowdot(sdot, wu[n][q][c], xr[t][c]);
+            sdot = pidev::warp_sum(sdot);
+            if (lane == 0) red_s[wid][t][q][n] = sdot;
+          }
+      __syncthreads();
+      if (tid < NB * GW) {
+        const int t = tid / GW, n = tid % GW;
+        if (n < n_here) {
+          const float bi = lb_s[w0 + n];
+          float su = 0.f, sg = 0.f;
+          for (int q = 0; q < kWarps; ++q) {   // fixed order over warps
+            su += red_s[q][t][0][n];
+            if (REGLU) sg += red_s[q][t][NR - 1][n];
+          }
+          if (FP8) {                           // row scales (staged slices)
+            const int k = list_s[w0 + n] - s0a;
+            su *= sc_up[k];
+            if (REGLU) sg *= sc_gate[k];
+          }
+          float a;
+          if (REGLU) {
+            const float gz = sg + bi;
+            a = (gz > 0.f ? gz : 0.f) * su;
+          } else {
+            const float z = su + bi;
+            a = z > 0.f ? z : 0.f;
+          }
+          a_all[t * p.slice_pad + w0 + n] = a;
+        }
+      }
+      __syncthreads();   // a of the window visible; red_s free for the next window
+#pragma unroll
+      for (int n = 0; n < GW; ++n) {
+        if (n < n_here) {
+#pragma unroll
+          for (int t = 0; t < NB; ++t) {
+            float an = a_all[t * p.slice_pad + w0 + n];
+            if (FP8) an *= sc_dn[list_s[w0 + n] - s0a];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) rowaxpy(acc[t][c], an, wd[n][c]);
+          }
+        }
+      }
+    }
+    } else {
+    // Two passes: all up-row dot products (a into shared memory), then all
+    // down rows, which were asked of L2 at the end of phase C and arrive
+    // while the up pass runs.
     for (int w0 = 0; w0 < lcount; w0 += GU) {
       const int n_here = min(GU, lcount - w0);
       RowVec wu[GU][NR][CPT];
@@ -599,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           }
         }
       }
+    }
     }
     PHASE_STAMP(l, 4);
     CTA_E_END(l, lcount);
