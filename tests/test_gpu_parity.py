@@ -185,6 +185,34 @@ def test_empty_set_and_bad_inputs(pi):
     assert layer.device_status() == 0
 
 
+def test_host_side_rejections_leave_the_gpu_untouched(pi):
+    """A bad permutation, a workspace that is too small and a batch beyond the
+    limit are refused on the host with an error code; the layer and the device
+    stay usable."""
+    d, ffn, r = 256, 512, 16
+    t, _ = _layer(LayerSpec(d=d, ffn=ffn, rank=r, mean_f=0.2), seed=41)
+    td = to_dev(t)
+    for bad in (np.r_[np.arange(ffn - 1), 0],          # a duplicate
+                np.r_[np.arange(ffn - 1), ffn],        # out of range
+                np.arange(ffn - 1)):                   # too short is read as ffn entries: pad with -1
+        perm = bad if bad.size == ffn else np.r_[bad, -1]
+        with pytest.raises(pi.PiError) as e:
+            pi.Layer.from_dict(td, perm=perm)
+        assert e.value.status == 1                     # PI_ERR_INVALID_ARG
+    layer = pi.Layer.from_dict(td)
+    x = make_tokens(d, 1, seed=1).cuda()
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pi.PiError) as e:
+        layer.forward(x, ws=small)
+    assert e.value.status == 1
+    with pytest.raises(pi.PiError) as e:
+        layer.forward(make_tokens(d, 129, seed=2).cuda())   # B > PI_MAX_BATCH
+    assert e.value.status == 1
+    y, idx, count = layer.forward(x)                   # still works
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all() and layer.device_status() == 0
+
+
 def test_permuted_layer(pi):
     d, ffn, r = 2048, 8192, 128
     t, L = _layer(LayerSpec(d=d, ffn=ffn, rank=r, mean_f=0.1), seed=37)
