@@ -7,6 +7,8 @@ Method: "PowerInfer" (egguo-blog reading report), section 2.3, core modules 3
 """
 from __future__ import annotations
 
+import math
+
 
 def _rows(a):
     if hasattr(a, "tolist"):
@@ -64,7 +66,14 @@ def forward(layer: dict, x) -> dict:
                 u = 0.0
                 for j in range(d):
                     u += Wu[i][j] * xb[j]
-                a = (z if z > 0.0 else 0.0) * u
+                if layer["act"] == "reglu":
+                    g = z if z > 0.0 else 0.0
+                elif z >= 0.0:                      # SiLU z / (1 + e^-z), written per sign
+                    g = z / (1.0 + math.exp(-z))
+                else:
+                    e = math.exp(z)
+                    g = z * e / (1.0 + e)
+                a = g * u
             for j in range(d):
                 y[j] += a * Wd[j][i]
         ys.append(y)

@@ -38,10 +38,10 @@ def _gamma(n: int) -> float:
 class OracleLayer:
     """One FFN layer in the index space it is given (model space or permuted).
 
-    act     "relu" or "reglu"
+    act     "relu", "reglu" or "swiglu"
     W_up    fp16 [ffn, d]   up projection (PyTorch Linear(d, ffn).weight layout)
     W_gate  fp16 [ffn, d]   gate projection (ReGLU only)
-    b       fp32 [ffn]      bias of the gated projection (up for ReLU, gate for ReGLU)
+    b       fp32 [ffn]      bias of the gated projection (up for ReLU, gate for ReGLU / SwiGLU)
     W_down  fp16 [d, ffn]   down projection (Linear(ffn, d).weight layout)
     W_p1    fp16 [r, d]     predictor first layer
     W_p2    fp16 [ffn, r]   predictor second layer
@@ -140,8 +140,19 @@ def logit_error_bound(L: OracleLayer, x, h=None) -> np.ndarray:
 # product that works directly on individual neurons).  For each neuron i of
 # the set S: ReLU   a_i = max(0, W_up_i . x + b_i)
 #            ReGLU  a_i = max(0, W_gate_i . x + b_i) * (W_up_i . x)
-# and y = sum over i in S (ascending) of a_i * W_down[:, i].
+#            SwiGLU a_i = SiLU(W_gate_i . x + b_i) * (W_up_i . x)
+# and y = sum over i in S (ascending) of a_i * W_down[:, i].  For SwiGLU the
+# set is a pruning choice (section 2.3, variable table: neurons that can be
+# skipped with a small effect on the output), so the sum over S differs from
+# the dense FFN by the skipped neurons' terms.
 # --------------------------------------------------------------------------
+
+def silu(z) -> np.ndarray:
+    """SiLU(z) = z * sigmoid(z) = z / (1 + e^-z), written per sign so that no
+    exponential overflows: z / (1 + e^-z) for z >= 0, z e^z / (1 + e^z) below."""
+    z = _f64(z)
+    e = np.exp(-np.abs(z))                       # in (0, 1]
+    return np.where(z >= 0, z / (1.0 + e), z * e / (1.0 + e))
 
 def _rowdots(W16: np.ndarray, rows: np.ndarray, xb: np.ndarray, chunk: int = 512) -> np.ndarray:
     """W[rows] . xb in float64, each row summed on its own (chunking over rows
@@ -164,6 +175,9 @@ def ffn_activations(L: OracleLayer, x, S) -> np.ndarray:
             a[t] = np.maximum(0.0, _rowdots(L.W_up, S, x[t]) + b)
         elif L.act == "reglu":
             g = np.maximum(0.0, _rowdots(L.W_gate, S, x[t]) + b)
+            a[t] = g * _rowdots(L.W_up, S, x[t])
+        elif L.act == "swiglu":
+            g = silu(_rowdots(L.W_gate, S, x[t]) + b)
             a[t] = g * _rowdots(L.W_up, S, x[t])
         else:
             raise ValueError(L.act)
@@ -200,10 +214,13 @@ def exact_mask(L: OracleLayer, x):
 
     ReLU sparsity is the share of neurons whose activation is exactly zero
     (section 2.3, variable table, "sparsity"); a neuron is active iff the
-    pre-activation of its gated projection is > 0 (up for ReLU, gate for ReGLU).
+    pre-activation of its gated projection is > 0 (up for ReLU, gate for
+    ReGLU).  For SwiGLU, whose activation is never exactly zero, the same
+    rule (the gate on SiLU's positive branch) serves the profile that orders
+    neurons hot-first.
     """
     x = _f64(x).reshape(-1, L.d)
-    Wg = L.W_gate if L.act == "reglu" else L.W_up
+    Wg = L.W_gate if L.act in ("reglu", "swiglu") else L.W_up
     z = x @ _f64(Wg).T + _f64(L.b)[None, :]
     return z > 0.0, z
 
@@ -211,7 +228,7 @@ def exact_mask(L: OracleLayer, x):
 def preact_error_bound(L: OracleLayer, x) -> np.ndarray:
     """Bound on |z_fp32 - z| for the gated pre-activation computed in binary32."""
     x = _f64(x).reshape(-1, L.d)
-    Wg = L.W_gate if L.act == "reglu" else L.W_up
+    Wg = L.W_gate if L.act in ("reglu", "swiglu") else L.W_up
     s = np.abs(x) @ np.abs(_f64(Wg)).T + np.abs(_f64(L.b))[None, :]
     return 2.0 * _gamma(L.d + 1) * s
 

@@ -291,3 +291,47 @@ def test_exact_arithmetic_mode(act):
         h32 = np.maximum(0, _fp32_sequential(L.W_p1, x32))
         l32 = _fp32_sequential(L.W_p2, h32, bias=L.c_p)
         np.testing.assert_array_equal(l32.astype(np.float64), r["l"][t_])
+
+
+# --------------------------------------------------------------------------
+# SwiGLU (a_i = SiLU(gate) * up over the kept neurons)
+# --------------------------------------------------------------------------
+
+def test_silu_closed_forms():
+    z = np.array([-50.0, -3.0, -1.0, 0.0, 0.5, 2.0, 40.0])
+    s = O.silu(z)
+    assert s[3] == 0.0
+    assert np.allclose(s - O.silu(-z), z, rtol=0, atol=1e-15)      # SiLU(z) - SiLU(-z) = z
+    assert np.allclose(s, z / (1.0 + np.exp(-z)), rtol=1e-15, atol=1e-300)
+    assert abs(s[-1] - 40.0) < 1e-15 and abs(s[0]) < 1e-20
+
+
+def test_swiglu_dense_matches_torch_modules():
+    spec = LayerSpec(d=48, ffn=40, rank=8, act="swiglu", mean_f=0.5)
+    t = make_layer(spec, 13, 0)
+    L = O.OracleLayer.from_tensors(t)
+    x = make_tokens(48, 3, seed=5)
+    gate = torch.nn.Linear(48, 40, dtype=torch.float64)
+    up = torch.nn.Linear(48, 40, bias=False, dtype=torch.float64)
+    down = torch.nn.Linear(40, 48, bias=False, dtype=torch.float64)
+    with torch.no_grad():
+        gate.weight.copy_(t["W_gate"].double()); gate.bias.copy_(t["b"].double())
+        up.weight.copy_(t["W_up"].double()); down.weight.copy_(t["W_down"].double())
+        ref = down(torch.nn.functional.silu(gate(x.double())) * up(x.double())).numpy()
+    assert np.allclose(O.dense_ffn(L, x), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_swiglu_sparse_sums_split_the_dense_sum_and_match_brute_force():
+    spec = LayerSpec(d=16, ffn=24, rank=4, act="swiglu", mean_f=0.5)
+    t = make_layer(spec, 17, 0)
+    L = O.OracleLayer.from_tensors(t)
+    x = make_tokens(16, 2, seed=9)
+    r = O.predicted_forward(L, x)
+    S = r["S"]
+    rest = np.setdiff1d(np.arange(24), S)
+    # the pruned neurons' terms are exactly what the sparse sum leaves out
+    assert np.allclose(O.sparse_ffn(L, x, S) + O.sparse_ffn(L, x, rest), O.dense_ffn(L, x),
+                       rtol=1e-12, atol=1e-14)
+    bf = brute.forward({k: (v.numpy() if hasattr(v, "numpy") else v) for k, v in t.items()}, x.numpy())
+    assert bf["S"] == list(S)
+    assert np.allclose(np.array(bf["y"]), r["y"], rtol=1e-12, atol=1e-14)

@@ -6,6 +6,8 @@ report, section 2.2 "Data source": OPT 7B-175B and Falcon-40B with ReLU,
 LLaMA2-70B with ReGLU) and for the decode setting of section 2.2 (inputs of
 8-128 tokens).  The firing-rate skew (Zipf exponent) and the mean sparsity
 stand in for the power-law activation locality of section 3.1, Finding 1.
+The SwiGLU shape follows section 4.4, limitation 1 (SwiGLU models keep about
+half of their neurons).
 """
 from __future__ import annotations
 
@@ -18,7 +20,7 @@ class LayerSpec:
     d: int                 # model width
     ffn: int               # number of FFN neurons
     rank: int              # predictor hidden width r
-    act: str = "relu"      # "relu" or "reglu"
+    act: str = "relu"      # "relu", "reglu" or "swiglu"
     alpha: float = 1.0     # Zipf exponent of the per-neuron firing rates
     mean_f: float = 0.10   # mean firing rate (1 - sparsity)
     f_cap: float = 0.9     # cap on any single neuron's firing rate
@@ -59,6 +61,13 @@ CONFIGS = (
         layer=LayerSpec(d=8192, ffn=28672, rank=512, act="reglu", alpha=0.8, mean_f=0.15),
         layers=16, tokens=256, seed=1003,
         description="LLaMA2-70B ReGLU-shaped FFN, d=8192, ffn=28672, 16 layers, r=512, batch 1",
+    ),
+    StackConfig(
+        name="llama2_70b_swiglu",
+        layer=LayerSpec(d=8192, ffn=28672, rank=512, act="swiglu", alpha=0.5, mean_f=0.5),
+        layers=16, tokens=256, seed=1006,
+        description="LLaMA2-70B SwiGLU-shaped FFN, d=8192, ffn=28672, 16 layers, r=512, batch 1, "
+                    "about 50% of the neurons kept by the predictor",
     ),
     StackConfig(
         name="falcon40b_stack",

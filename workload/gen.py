@@ -109,14 +109,14 @@ def make_layer(spec: LayerSpec, base_seed: int, layer: int = 0,
     """One synthetic layer in model space (PyTorch Linear weight layouts).
 
     Returns W_up [ffn,d], W_gate [ffn,d] or None, b [ffn] fp32 (bias of the
-    gated projection: up for ReLU, gate for ReGLU), W_down [d,ffn],
+    gated projection: up for ReLU, gate for ReGLU / SwiGLU), W_down [d,ffn],
     W_p1 [r,d], W_p2 [ffn,r], c_p [ffn] fp32 or None, and f [ffn] float64
     (the target firing rates, on the CPU).
     """
     d, ffn, r = spec.d, spec.ffn, spec.rank
     S = lambda name: sub_seed(base_seed, layer, name)  # noqa: E731
     W_up = _randn_half((ffn, d), spec.w_std, device, S("W_up"))
-    W_gate = _randn_half((ffn, d), spec.w_std, device, S("W_gate")) if spec.act == "reglu" else None
+    W_gate = _randn_half((ffn, d), spec.w_std, device, S("W_gate")) if spec.act in ("reglu", "swiglu") else None
     W_down = _randn_half((d, ffn), spec.w_std, device, S("W_down"))
     W_p1 = _randn_half((r, d), spec.wp_std, device, S("W_p1"))
     W_p2 = _randn_half((ffn, r), spec.wp_std, device, S("W_p2"))
@@ -158,7 +158,7 @@ def make_exact_layer(d: int, ffn: int, r: int, act: str = "relu", seed: int = 7,
                      p_nz: float = 0.25) -> Dict[str, Optional[torch.Tensor]]:
     S = lambda name: sub_seed(seed, 0, "exact/" + name)  # noqa: E731
     W_up = _ternary((ffn, d), p_nz, 0.125, S("W_up"))
-    W_gate = _ternary((ffn, d), p_nz, 0.125, S("W_gate")) if act == "reglu" else None
+    W_gate = _ternary((ffn, d), p_nz, 0.125, S("W_gate")) if act in ("reglu", "swiglu") else None
     W_down = _ternary((d, ffn), p_nz, 0.125, S("W_down"))
     W_p1 = _ternary((r, d), p_nz, 0.125, S("W_p1"))
     W_p2 = _ternary((ffn, r), p_nz, 0.125, S("W_p2"))
