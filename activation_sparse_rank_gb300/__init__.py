@@ -7,6 +7,7 @@ libpi.so has not been built (``python activation_sparse_rank_gb300/_build.py``).
 """
 from .binding import (  # noqa: F401
     PI_ACT_REGLU,
+    PI_ACT_SWIGLU,
     PI_ACT_RELU,
     PI_MAX_BATCH,
     Layer,
@@ -23,6 +24,7 @@ __all__ = [
     "PiError",
     "PI_ACT_RELU",
     "PI_ACT_REGLU",
+    "PI_ACT_SWIGLU",
     "PI_MAX_BATCH",
     "hot_first_perm",
     "lib",

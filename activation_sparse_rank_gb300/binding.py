@@ -29,6 +29,8 @@ lib = C.CDLL(str(lib_path))
 PI_OK = 0
 PI_ACT_RELU = 0
 PI_ACT_REGLU = 1
+PI_ACT_SWIGLU = 2
+_ACTS = {"relu": PI_ACT_RELU, "reglu": PI_ACT_REGLU, "swiglu": PI_ACT_SWIGLU}
 PI_MAX_BATCH = 128
 PI_ROWS_FP16 = 0
 PI_ROWS_FP8_E4M3 = 1
@@ -108,7 +110,9 @@ def _req(t: torch.Tensor, dtype, name: str):
 
 
 def make_desc(W_up, W_gate, b, W_down, W_p1, W_p2, c_p, act, rows="fp16") -> pi_layer_desc:
-    act_id = PI_ACT_REGLU if act in ("reglu", PI_ACT_REGLU) else PI_ACT_RELU
+    act_id = act if isinstance(act, int) else _ACTS.get(act)
+    if act_id not in _ACTS.values():
+        raise ValueError(f"act must be one of {sorted(_ACTS)}, not {act!r}")
     _req(W_up, torch.float16, "W_up")
     ffn, d = W_up.shape
     rank = W_p1.shape[0]
@@ -142,7 +146,7 @@ class Layer:
                                    None if perm_arr is None else perm_arr.ctypes.data_as(C.c_void_p),
                                    _stream(stream)), "pi_layer_create")
         self.d, self.ffn, self.rank = int(desc.d), int(desc.ffn), int(desc.rank)
-        self.act = "reglu" if desc.act == PI_ACT_REGLU else "relu"
+        self.act = {v: k for k, v in _ACTS.items()}[int(desc.act)]
         self.rows = rows
         self.device = W_up.device
 

@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(256) k_profile(const __half *__restrict__ W,
 
 pi_status check_desc(const pi_layer_desc *D) {
   if (!D) return pi::fail(PI_ERR_INVALID_ARG, "desc is NULL");
-  if (D->act != PI_ACT_RELU && D->act != PI_ACT_REGLU)
-    return pi::fail(PI_ERR_INVALID_ARG, "act %d is neither PI_ACT_RELU nor PI_ACT_REGLU", D->act);
+  if (D->act != PI_ACT_RELU && D->act != PI_ACT_REGLU && D->act != PI_ACT_SWIGLU)
+    return pi::fail(PI_ERR_INVALID_ARG, "act %d is not PI_ACT_RELU, PI_ACT_REGLU or PI_ACT_SWIGLU", D->act);
   if (D->d < 8 || D->d > PI_MAX_D || D->d % 8)
     return pi::fail(PI_ERR_UNSUPPORTED, "d=%d: need 8 <= d <= %d and d %% 8 == 0", D->d, PI_MAX_D);
   if (D->rank < 8 || D->rank > PI_MAX_RANK || D->rank % 8)
@@ -151,8 +151,8 @@ pi_status check_desc(const pi_layer_desc *D) {
     return pi::fail(PI_ERR_UNSUPPORTED, "ffn=%d: need 1 <= ffn <= %d", D->ffn, PI_MAX_FFN);
   if (!D->W_up || !D->b || !D->W_down || !D->W_p1 || !D->W_p2)
     return pi::fail(PI_ERR_INVALID_ARG, "a required weight pointer is NULL");
-  if ((D->act == PI_ACT_REGLU) != (D->W_gate != nullptr))
-    return pi::fail(PI_ERR_INVALID_ARG, "W_gate must be given exactly when act is PI_ACT_REGLU");
+  if ((D->act != PI_ACT_RELU) != (D->W_gate != nullptr))
+    return pi::fail(PI_ERR_INVALID_ARG, "W_gate must be given exactly for a gated act (ReGLU, SwiGLU)");
   if (D->row_format != PI_ROWS_FP16 && D->row_format != PI_ROWS_FP8_E4M3)
     return pi::fail(PI_ERR_INVALID_ARG, "row_format %d is neither PI_ROWS_FP16 nor PI_ROWS_FP8_E4M3",
                     D->row_format);
@@ -224,7 +224,7 @@ cudaError_t record_hook(cudaEvent_t ev, cudaStream_t s) {
 
 cudaError_t run_profile(const pi_layer_desc *D, const __half *x, int T, int32_t *counts,
                         cudaStream_t s) {
-  const __half *W = reinterpret_cast<const __half *>(D->act == PI_ACT_REGLU ? D->W_gate : D->W_up);
+  const __half *W = reinterpret_cast<const __half *>(D->act != PI_ACT_RELU ? D->W_gate : D->W_up);
   const int tiles_t = (T + 63) / 64;
   const int max_y = 65535;
   for (int ty0 = 0; ty0 < tiles_t; ty0 += max_y) {
@@ -313,11 +313,12 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   // the gathered rows: fp16, or E4M3 codes (1 byte) plus one scale per row
   const size_t rowmat = q8 ? (size_t)ffn * d : wrow;
   const size_t o_up = off; off += align_up(rowmat);
-  const size_t o_gate = off; if (D->act == PI_ACT_REGLU) off += align_up(rowmat);
+  const bool gated = D->act != PI_ACT_RELU;
+  const size_t o_gate = off; if (gated) off += align_up(rowmat);
   const size_t o_dT = off; off += align_up(rowmat);
   const size_t vsc = q8 ? align_up((size_t)ffn * sizeof(float)) : 0;
   const size_t o_sup = off; off += vsc;
-  const size_t o_sgate = off; if (D->act == PI_ACT_REGLU) off += vsc;
+  const size_t o_sgate = off; if (gated) off += vsc;
   const size_t o_sdT = off; off += vsc;
   const size_t o_b = off; off += align_up((size_t)ffn * sizeof(float));
   const size_t o_c = off; off += align_up((size_t)ffn * sizeof(float));
@@ -339,14 +340,14 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   L->W_p2 = reinterpret_cast<__half *>(b + o_p2);
   if (!q8) {
     L->W_up = reinterpret_cast<__half *>(b + o_up);
-    L->W_gate = D->act == PI_ACT_REGLU ? reinterpret_cast<__half *>(b + o_gate) : nullptr;
+    L->W_gate = gated ? reinterpret_cast<__half *>(b + o_gate) : nullptr;
     L->W_dT = reinterpret_cast<__half *>(b + o_dT);
   } else {
     L->Q_up = reinterpret_cast<uint8_t *>(b + o_up);
-    L->Q_gate = D->act == PI_ACT_REGLU ? reinterpret_cast<uint8_t *>(b + o_gate) : nullptr;
+    L->Q_gate = gated ? reinterpret_cast<uint8_t *>(b + o_gate) : nullptr;
     L->Q_dT = reinterpret_cast<uint8_t *>(b + o_dT);
     L->s_up = reinterpret_cast<float *>(b + o_sup);
-    L->s_gate = D->act == PI_ACT_REGLU ? reinterpret_cast<float *>(b + o_sgate) : nullptr;
+    L->s_gate = gated ? reinterpret_cast<float *>(b + o_sgate) : nullptr;
     L->s_dT = reinterpret_cast<float *>(b + o_sdT);
   }
   L->b = reinterpret_cast<float *>(b + o_b);
@@ -389,7 +390,7 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_up), q8 ? tmp : L->W_up,
                                            perm_dev, ffn, d);
   if (q8) k_quantize_rows<<<grid_q, 256, 0, s>>>(tmp, L->Q_up, L->s_up, ffn, d);
-  if (D->act == PI_ACT_REGLU) {
+  if (gated) {
     k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_gate), q8 ? tmp : L->W_gate,
                                              perm_dev, ffn, d);
     if (q8) k_quantize_rows<<<grid_q, 256, 0, s>>>(tmp, L->Q_gate, L->s_gate, ffn, d);

@@ -88,6 +88,7 @@ struct StackParams {
   int off_flag, off_list, off_lb, off_a, off_stage, stage_bytes, slice_pad;   // shared memory layout
   int soff_c, soff_b, soff_p1, soff_p2;                     // offsets inside a stage buffer
   int soff_su, soff_sg, soff_sd;                            // row-scale slices (FP8 layers)
+  int gate_silu;                                            // gated layers: SiLU gate (SwiGLU)
   const __half *x;       // [n_layers, B, d]
   float *y;              // [n_layers, B, d]
   int32_t *count;        // [n_layers] or nullptr
@@ -246,6 +247,11 @@ __device__ __forceinline__ uint2 ld_stream2(const uint2 *p) {
   uint2 v;
   asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
+}
+
+// Gate of a gated neuron: ReLU (ReGLU) or SiLU (SwiGLU).
+__device__ __forceinline__ float gate_act(float z, bool silu) {
+  return silu ? z / (1.0f + expf(-z)) : (z > 0.f ? z : 0.f);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           float a;
           if (REGLU) {
             const float gz = sg + bi;
-            a = (gz > 0.f ? gz : 0.f) * su;
+            a = pidev::gate_act(gz, p.gate_silu != 0) * su;
           } else {
             const float z = su + bi;
             a = z > 0.f ? z : 0.f;
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           float a;
           if (REGLU) {
             const float gz = sg + bi;
-            a = (gz > 0.f ? gz : 0.f) * su;
+            a = pidev::gate_act(gz, p.gate_silu != 0) * su;
           } else {
             const float z = su + bi;
             a = z > 0.f ? z : 0.f;
@@ -838,7 +838,7 @@ SmemPlan smem_plan(const pi_layer *L, int B) {
   const bool q8 = L->row_format == PI_ROWS_FP8_E4M3;
   const size_t sc = q8 ? sizeof(float) * (slice + 8) : 0;
   s.soff_su = so;    so = align128(so + sc);
-  s.soff_sg = so;    so = align128(so + (L->act == PI_ACT_REGLU ? sc : 0));
+  s.soff_sg = so;    so = align128(so + (L->act != PI_ACT_RELU ? sc : 0));
   s.soff_sd = so;    so = align128(so + sc);
   s.stage_small = so;
   s.soff_p1 = so;    so = align128(so + na_max * L->d * 2);
@@ -893,7 +893,7 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   int GL = 32;
   while (GL > 8 && GL * 8 > L0->rank) GL >>= 1;
   p.lanes_l = GL;
-  const int rows_per_neuron = L0->act == PI_ACT_REGLU ? 3 : 2;
+  const int rows_per_neuron = L0->act != PI_ACT_RELU ? 3 : 2;
   // early L2 prefetch of the local active rows: up to ~768 KB of rows per CTA
   const int rb = L0->row_format == PI_ROWS_FP8_E4M3 ? L0->d : 2 * L0->d;   // bytes of a gathered row
   const int pf = (768 * 1024) / (rb * rows_per_neuron);
@@ -924,7 +924,8 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   cudaError_t e = cudaMemsetAsync(p.bar, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
   const size_t smem = step_smem(L0, B);
-  const bool reglu = L0->act == PI_ACT_REGLU;
+  const bool reglu = L0->act != PI_ACT_RELU;      // gated: ReGLU or SwiGLU
+  p.gate_silu = L0->act == PI_ACT_SWIGLU ? 1 : 0;
   const bool q8 = L0->row_format == PI_ROWS_FP8_E4M3;
   e = record_hook(L0->ev_before, s);
   if (e != cudaSuccess) return e;

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(512) k_fused_small(
     const float *__restrict__ bias, const __half *__restrict__ W_dT,
     const __half *__restrict__ x, int d, int ffn, const int32_t *__restrict__ idx,
     const int32_t *__restrict__ count_p, int count_const, int sub,
-    float *__restrict__ partial, unsigned int *status) {
+    float *__restrict__ partial, unsigned int *status, int silu) {
   constexpr int G = FusedShape<CPT, REGLU>::G;
   constexpr int NR = REGLU ? 2 : 1;
   __shared__ float red_s[16][NB][NR][kWinMax];
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(512) k_fused_small(
         }
         if (REGLU) {
           const float gz = sg + bias[i];
-          a = (gz > 0.f ? gz : 0.f) * su;
+          a = pidev::gate_act(gz, silu != 0) * su;
         } else {
           const float z = su + bias[i];
           a = z > 0.f ? z : 0.f;
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(256) k_sparse_up(
     const __half *__restrict__ W_up, const __half *__restrict__ W_gate,
     const float *__restrict__ bias, const __half *__restrict__ x, int B, int d, int ffn,
     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p, int count_const,
-    float *__restrict__ a, unsigned int *status) {
+    float *__restrict__ a, unsigned int *status, int silu) {
   pidev::griddep_wait();
   pidev::griddep_launch();
   const int lane = threadIdx.x & 31;
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(256) k_sparse_up(
           if (ok) {
             if (REGLU) {
               const float gz = g + bias[i];
-              av = (gz > 0.f ? gz : 0.f) * u;
+              av = pidev::gate_act(gz, silu != 0) * u;
             } else {
               const float z = u + bias[i];
               av = z > 0.f ? z : 0.f;
@@ -361,7 +361,7 @@ cudaError_t launch_fused(const pi_layer *L, const __half *x, const int32_t *idx,
   if (sub < 1) sub = 1;
   return pi::launch_pdl(k_fused_small<CPT, NB, REGLU>, dim3(nsplit), dim3(threads), 0, s,
                         L->W_up, L->W_gate, L->b, L->W_dT, x, L->d, L->ffn, idx, count,
-                        count_const, sub, partial, L->status);
+                        count_const, sub, partial, L->status, L->act == PI_ACT_SWIGLU ? 1 : 0);
 }
 
 template <int NB, bool REGLU>
@@ -405,7 +405,8 @@ cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int3
                            char *ws, cudaStream_t s) {
   if (B > 2 && tc_supported(L, B)) return run_sparse_ffn_tc(L, x, B, idx, count, count_const, y, w, ws, s);
   float *partial = reinterpret_cast<float *>(ws + w.partial);
-  const bool reglu = L->act == PI_ACT_REGLU;
+  const bool reglu = L->act != PI_ACT_RELU;      // gated: ReGLU or SwiGLU
+  const int silu = L->act == PI_ACT_SWIGLU ? 1 : 0;
   cudaError_t e;
   int nsplit;
   if (B <= 2) {
@@ -426,10 +427,10 @@ cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int3
     e = record_hook(L->ev_before, s);
     if (e != cudaSuccess) return e;
     e = reglu ? launch_pdl(k_sparse_up<true>, dim3(grid_up), dim3(256), 0, s, L->W_up, L->W_gate,
-                           L->b, x, B, L->d, L->ffn, idx, count, count_const, a, L->status)
+                           L->b, x, B, L->d, L->ffn, idx, count, count_const, a, L->status, silu)
               : launch_pdl(k_sparse_up<false>, dim3(grid_up), dim3(256), 0, s, L->W_up,
                            L->W_gate, L->b, x, B, L->d, L->ffn, idx, count, count_const, a,
-                           L->status);
+                           L->status, silu);
     if (e != cudaSuccess) return e;
     nsplit = down_splits(L, B);
     e = launch_pdl(k_sparse_down, dim3(nsplit, down_colblocks(L)), dim3(256), 0, s, L->W_dT,

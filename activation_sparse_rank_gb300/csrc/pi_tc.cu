@@ -195,7 +195,9 @@ __device__ __forceinline__ int tile_row(const int32_t *idx, int k, int count, in
 // and kHidden only token columns [c_begin, c_end) are produced.
 template <int MODE, bool REGLU, typename F>
 __device__ __forceinline__ bool row_epilogue(F fetch8, int c_begin, int c_end, int i, int kq, float bi, int B,
-                                             int Bp, int Nmma, __half *abuf, int abuf_ld, uint8_t *mask_out) {
+                                             int Bp, int Nmma, __half *abuf, int abuf_ld, uint8_t *mask_out,
+                                             bool silu) {
+  // silu: the gate of a gated (kAct, REGLU) row is SiLU (SwiGLU) instead of ReLU
   if (MODE == kLogits) {                // kLogits: token columns [c_begin, c_end); returns l > 0 for one of them
     bool on = false;
     for (int c0 = c_begin; c0 < c_end; c0 += 8) {
@@ -219,7 +221,7 @@ __device__ __forceinline__ bool row_epilogue(F fetch8, int c_begin, int c_end, i
         float a = 0.f;
         if (i >= 0 && b < B) {
           const float z = g8[j] + bi;
-          a = REGLU ? (z > 0.f ? z : 0.f) * u8[j] : (z > 0.f ? z : 0.f);
+          a = REGLU ? pidev::gate_act(z, silu) * u8[j] : (z > 0.f ? z : 0.f);
         }
         const __half hi = __float2half_rn(a);
         const __half lo = __float2half_rn(a - __half2float(hi));
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
                                                     int B, int Bp, int nstage, int kw, __half *__restrict__ abuf,
                                                     int abuf_ld, float *__restrict__ piece,
                                                     uint8_t *__restrict__ mask_out, int32_t *__restrict__ tile_cnt,
-                                                    unsigned int *status) {
+                                                    unsigned int *status, int silu) {
   // d: row length of W and contraction length K; ffn: number of rows of W.
   // A pipeline stage holds kw consecutive 64-element K slabs, so every
   // gathered row contributes kw * 128 contiguous bytes per stage.
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
       const int i = rows_s[q];
       const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
       const bool on = row_epilogue<MODE, REGLU>([&](int c, float *v) { tmem_ld8(trow + (uint32_t)c, v); }, 0, Bp,
-                                                i, k0 + q, bi, B, Bp, Nmma, abuf, abuf_ld, mask_out);
+                                                i, k0 + q, bi, B, Bp, Nmma, abuf, abuf_ld, mask_out, silu != 0);
       if (MODE == kLogits) {            // active rows of the tile, for the ordered compaction
         const int n_on = __syncthreads_count(on && i >= 0);
         if (tid == 0) tile_cnt[tile] = n_on;
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(1024) k_tc_fixup(const float *__restrict__ pie
                                                    const float *__restrict__ bias, int ffn, int B, int Bp, int KT,
                                                    int grid, __half *__restrict__ abuf, int abuf_ld,
                                                    uint8_t *__restrict__ mask_out, int32_t *__restrict__ tile_cnt,
-                                                   unsigned int *status) {
+                                                   unsigned int *status, int silu) {
   constexpr int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const int ncolD = NA * Nmma;
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(1024) k_tc_fixup(const float *__restrict__ pie
   bool on = false;
   for (int c0 = 8 * grp; c0 < Bp; c0 += 8 * ngrp)
     on |= row_epilogue<MODE, REGLU>(fetch8, c0, c0 + 8, i, tile * kTile + q, bi, B, Bp, Nmma, abuf, abuf_ld,
-                                    nullptr);
+                                    nullptr, silu != 0);
   if (MODE == kLogits) {
     on_s[grp][q] = on ? 1 : 0;
     __syncthreads();
@@ -770,7 +772,7 @@ template <int MODE, bool REGLU>
 cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, const CUtensorMap &tm_x,
                         const int32_t *idx, const int32_t *count, int count_const, const float *bias, int K,
                         int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, float *piece,
-                        int32_t *tile_cnt, bool rows_known, cudaStream_t s) {
+                        int32_t *tile_cnt, bool rows_known, cudaStream_t s, int silu = 0) {
   const int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const size_t sub = NA * (size_t)kTile * 128 + (((size_t)Nmma * 128 + 1023) & ~(size_t)1023);
@@ -792,12 +794,12 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<G, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, kw, out, out_ld,
-                            piece, mask, tile_cnt, L->status);
+                            piece, mask, tile_cnt, L->status, silu);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int groups = std::min(Bp / 8, 8);       // 128 threads per group of token columns
   k_tc_fixup<MODE, REGLU><<<G, kTile * groups, 0, s>>>(piece, idx, count, count_const, bias, nrows, B, Bp,
-                                                       slabs / kw, G, out, out_ld, mask, tile_cnt, L->status);
+                                                       slabs / kw, G, out, out_ld, mask, tile_cnt, L->status, silu);
   return cudaGetLastError();
 }
 
@@ -849,7 +851,8 @@ cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *m
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,
                               char *ws, cudaStream_t s) {
-  const bool reglu = L->act == PI_ACT_REGLU;
+  const bool reglu = L->act != PI_ACT_RELU;      // gated: ReGLU or SwiGLU
+  const int silu = L->act == PI_ACT_SWIGLU ? 1 : 0;
   const int Bp = tc_bpad(B);
   const int ffn_pad = tc_ffn_pad(L);
   __half *abuf = reinterpret_cast<__half *>(ws + w.abuf);
@@ -863,7 +866,7 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   cudaError_t e = record_hook(L->ev_before, s);
   if (e != cudaSuccess) return e;
   e = reglu ? launch_rows<kAct, true>(L, L->W_gate, L->W_up, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
-                                      Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s)
+                                      Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s, silu)
             : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
                                        Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s);
   if (e != cudaSuccess) return e;

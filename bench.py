@@ -68,7 +68,7 @@ def bytes_per_active_neuron(d: int, act: str, rows: str = "fp16") -> int:
     """Weight bytes read per active neuron: its up row (+ gate row) and its
     W_down^T row, 2d bytes each (fp8 rows: d code bytes + a 4-byte scale)."""
     per_row = d + 4 if rows == "fp8" else 2 * d
-    return per_row * (3 if act == "reglu" else 2)
+    return per_row * (3 if act in ("reglu", "swiglu") else 2)
 
 
 def predictor_bytes(d: int, ffn: int, r: int) -> int:
@@ -431,7 +431,7 @@ def main():
                 "algorithmic_bytes_per_launch": alg_bytes / len(k_ms),
                 "timing": how}
     if Bt > 2:
-        mult = 3 if spec.act == "reglu" else 2
+        mult = 3 if spec.act in ("reglu", "swiglu") else 2
         flops = 2.0 * Bt * float(cnt[:, 0].sum()) * spec.d * mult / len(k_ms)
         roofline["tensor_tflops"] = flops / (k_avg_ms / 1e3) / 1e12
 

@@ -47,7 +47,11 @@ typedef enum {
 
 typedef enum {
   PI_ACT_RELU = 0,   /* a_i = max(0, W_up_i.x + b_i)                           */
-  PI_ACT_REGLU = 1   /* a_i = max(0, W_gate_i.x + b_i) * (W_up_i.x)            */
+  PI_ACT_REGLU = 1,  /* a_i = max(0, W_gate_i.x + b_i) * (W_up_i.x)            */
+  PI_ACT_SWIGLU = 2  /* a_i = SiLU(W_gate_i.x + b_i) * (W_up_i.x), SiLU(z) = z / (1 + e^-z):
+                        section 2.3 variable table and section 4.4 limitation 1 (SwiGLU
+                        models: neurons pruned with a small effect, about half kept); the
+                        sum runs over the predicted set, which skips the pruned neurons */
 } pi_act;
 
 /* Storage of the up / gate / down rows that the sparse operators gather.
@@ -76,8 +80,8 @@ typedef struct pi_layer pi_layer;
 /* One FFN layer in model space, PyTorch nn.Linear weight layouts, all device
  * pointers.  Read only during pi_layer_create / pi_profile_activations.
  *   W_up   [ffn, d]   fp16  up projection
- *   W_gate [ffn, d]   fp16  gate projection (PI_ACT_REGLU only, else NULL)
- *   b      [ffn]      fp32  bias of the gated projection (up for ReLU, gate for ReGLU)
+ *   W_gate [ffn, d]   fp16  gate projection (PI_ACT_REGLU / PI_ACT_SWIGLU, else NULL)
+ *   b      [ffn]      fp32  bias of the gated projection (up for ReLU, gate otherwise)
  *   W_down [d, ffn]   fp16  down projection
  *   W_p1   [rank, d]  fp16  predictor first layer (no bias)
  *   W_p2   [ffn, rank] fp16 predictor second layer
