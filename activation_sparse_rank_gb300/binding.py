@@ -32,6 +32,7 @@ PI_ACT_REGLU = 1
 PI_ACT_SWIGLU = 2
 _ACTS = {"relu": PI_ACT_RELU, "reglu": PI_ACT_REGLU, "swiglu": PI_ACT_SWIGLU}
 PI_MAX_BATCH = 128
+PI_STACK_LAYERS_PER_LAUNCH = 32   # include/pi.h
 PI_ROWS_FP16 = 0
 PI_ROWS_FP8_E4M3 = 1
 

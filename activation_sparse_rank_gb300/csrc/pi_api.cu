@@ -666,9 +666,15 @@ pi_status pi_layer_set_hot_count(pi_layer *L, int32_t n_hot) {
 
 int32_t pi_forward_launches(const pi_layer *L, int32_t B) {
   if (!L || B < 1 || B > PI_MAX_BATCH) return 0;
-  // B <= 2: one persistent cooperative launch (after a barrier-counter memset);
-  // otherwise predict_h, predict_l, compact, up, down, reduce
-  return B <= 2 ? 1 : 6;   // (tensor-core path: up, down, reduce; ALU path likewise)
+  // B <= 2: the persistent step and the ordered compaction of its masks
+  // (memsets not counted).  Otherwise, on the tensor cores: hidden layer and
+  // logits (each with its split-tile fix-up), tile compaction, up (+ fix-up),
+  // down, column reduce; the predictor on the ALU instead: predict_h,
+  // predict_l, compact; without tensor cores: predictor, compact, up, down,
+  // reduce.
+  if (B <= 2) return 2;
+  if (!pi::tc_supported(L, B)) return 6;
+  return pi::tc_predict_supported(L, B) ? 9 : 7;
 }
 
 pi_status pi_device_status(pi_layer *L, void *stream) {

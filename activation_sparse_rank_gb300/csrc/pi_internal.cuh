@@ -69,7 +69,7 @@ struct WsLayout {
 };
 
 // Layers per persistent launch (longer stacks are split into several launches).
-constexpr int kMaxStack = 32;
+constexpr int kMaxStack = PI_STACK_LAYERS_PER_LAUNCH;
 
 
 // Device pointers of one layer, as the persistent kernel sees them.

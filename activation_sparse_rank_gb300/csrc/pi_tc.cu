@@ -82,15 +82,6 @@ __device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap *map,
       : "memory");
 }
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, int r0, int r1, int r2,
-                                            int r3, uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
-          dst),
-      "l"(map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar)
-      : "memory");
-}
-
 // 16-byte global -> shared copy (L2 only), and an mbarrier arrival once all of
 // this thread's earlier copies have landed (counted against the init count).
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src) {

@@ -14,7 +14,7 @@ from typing import List, Optional
 
 import torch
 
-from .binding import Layer, stack_forward
+from .binding import PI_STACK_LAYERS_PER_LAUNCH, Layer, stack_forward
 
 
 class SparseFFNStack:
@@ -44,7 +44,7 @@ class SparseFFNStack:
     def launches_per_step(self) -> int:
         """Kernels of this library launched per step (memsets not counted)."""
         if self.B <= 2:
-            n_launch = -(-self.L // 64)
+            n_launch = -(-self.L // PI_STACK_LAYERS_PER_LAUNCH)
             return (2 if self.want_idx else 1) * n_launch * self.T
         return sum(l.forward_launches(self.B) for l in self.layers) * self.T
 

@@ -412,7 +412,7 @@ def main():
         kname = f"k_stack_step (one token through {n_layers} layers)"
     else:         # tensor-core up + down of layer 0: its active rows
         alg_bytes = float(cnt[:, 0].sum()) * bytes_per_active_neuron(spec.d, spec.act)
-        kname = "k_tc_up + k_tc_down (layer 0, tcgen05)"
+        kname = "k_tc_rows<act> + k_tc_down (layer 0, tcgen05)"
     k_avg_ms = sum(k_ms) / len(k_ms)
     achieved = alg_bytes / len(k_ms) / (k_avg_ms / 1e3) / 1e9
     traffic = None

@@ -74,6 +74,8 @@ typedef enum {
 #define PI_MAX_RANK   2048    /* rank % 8 == 0 */
 #define PI_MAX_FFN    (1 << 20)
 #define PI_MAX_BATCH  128
+/* pi_stack_forward runs one persistent kernel per this many layers (1-2 tokens). */
+#define PI_STACK_LAYERS_PER_LAUNCH 32
 
 typedef struct pi_layer pi_layer;
 

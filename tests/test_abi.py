@@ -76,3 +76,13 @@ def test_rejections_before_any_launch(pi):
     assert lib.pi_workspace_bytes(None, 1) == 0
     assert lib.pi_hot_first_perm(None, 4, None) == 1
     assert lib.pi_layer_destroy(None) == 0
+
+
+def test_binding_constants_match_the_header(pi):
+    text = (ROOT / "include" / "pi.h").read_text()
+    defs = dict(re.findall(r"#define\s+(PI_[A-Z_]+)\s+\(?([0-9]+)", text))
+    assert int(defs["PI_MAX_BATCH"]) == pi.binding.PI_MAX_BATCH
+    assert int(defs["PI_STACK_LAYERS_PER_LAUNCH"]) == pi.binding.PI_STACK_LAYERS_PER_LAUNCH
+    enums = dict(re.findall(r"\b(PI_(?:ACT|ROWS)_[A-Z0-9_]+)\s*=\s*([0-9]+)", text))
+    for name, value in enums.items():
+        assert getattr(pi.binding, name) == int(value), name
