@@ -193,14 +193,19 @@ def run_reference(args, cfg):
         return
     spec = cfg.layer
     n_layers = 2
+    Bt = args.batch
+    L_total = args.layers or cfg.layers
     host_layers = [{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
                     for k, v in make_layer(spec, cfg.seed, l, device="cpu").items()}
                    for l in range(n_layers)]
     T = max(4, args.steps + args.warmup) * 2
-    X = make_tokens(spec.d, T * n_layers, sub_seed(cfg.seed, 0, "bench_x"), "cpu").view(T, n_layers, 1, spec.d)
+    X = make_tokens(spec.d, T * n_layers * Bt, sub_seed(cfg.seed, 0, "bench_x"), "cpu").view(T, n_layers, Bt, spec.d)
     per_step = max(1.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
     from oracle import ffn as O
     OL = [O.OracleLayer.from_tensors(t) for t in host_layers]
+    if args.rows == "fp8":                       # the FFN of the E4M3 rows
+        from oracle import quant as Q
+        OL = [Q.fp8_layer(L) for L in OL]
 
     def one_step(tok0):
         t0 = time.perf_counter()
@@ -223,18 +228,18 @@ def run_reference(args, cfg):
         el, p, tok = one_step(tok)
         tot_t += el
         tot_p += p
-    value = 1.0 / ((tot_t / tot_p) * cfg.layers)
+    value = Bt / ((tot_t / tot_p) * L_total)
     cores = os.cpu_count()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(cfg, args.layers or cfg.layers, args.tokens or cfg.tokens, 1,
-                                  int(os.environ.get("WORLD_SIZE", "1"))),
+        "config": workload_config(cfg, L_total, args.tokens or cfg.tokens, Bt,
+                                  int(os.environ.get("WORLD_SIZE", "1")), args.rows),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{tot_p} (token, layer) pairs of layers 0..{n_layers - 1}, "
-                                   f"{tot_t:.1f} s, scaled to a {cfg.layers}-layer stack; numpy "
+                                   f"{tot_t:.1f} s, batch {Bt}, scaled to a {L_total}-layer stack; numpy "
                                    f"float64 with its default BLAS threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
