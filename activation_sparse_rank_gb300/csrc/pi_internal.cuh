@@ -85,6 +85,7 @@ struct LayerDev {
 struct StackParams {
   int n_layers, d, ffn, rank;
   int G, staged, lanes_l, pf_rows, pf_next;
+  int lgt_s;                     // log2 threads per staged W_p2 row (logits)
   int off_flag, off_list, off_lb, off_a, off_stage, stage_bytes, slice_pad;   // shared memory layout
   int soff_c, soff_b, soff_p1, soff_p2;                     // offsets inside a stage buffer
   int soff_su, soff_sg, soff_sd;                            // row-scale slices (FP8 layers)

@@ -14,8 +14,8 @@
 //   C  l = W_p2 h + c_p over the CTA's slice, threshold, ordered local list
 //   E  the CTA streams the up/gate/down rows of its own active neurons (bulk
 //      L2 prefetch of all of them first, then 16-byte loads in windows), forms
-//      a and its partial y; meanwhile the next layer's predictor weights are
-//      staged into shared memory by TMA (or prefetched into L2 when too big)
+//      a and its partial y; meanwhile the next layer's predictor weights land
+//      in shared memory by TMA (or are prefetched into L2 when too big)
 //   -- barrier 2 (partials complete)
 //   F  y = sum of the G partials in a fixed order (deterministic)
 //   -- barrier 3 (y complete: the next layer may depend on it, as in decode)
@@ -257,20 +257,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // layer l's inputs go to buffer l & 1: layer 0's now, layer l + 1's at the
+  // start of layer l (buffer (l + 1) & 1 is free since the last barrier)
   if (tid == kIssuer) stage(0);
+  // on a failed wait: let the stage copies this CTA may have in flight land
+  auto drain = [&](int first, int last) {
+    for (int k = first; k <= last && k < p.n_layers; ++k)
+      mbar_wait(mbar0 + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1));
+  };
 
   for (int l = 0; l < p.n_layers; ++l) {
     const pi::LayerDev &Ld = p.layers[l];
     PHASE_STAMP(l, 0);
 
     const uint32_t mbar = mbar0 + 8u * (uint32_t)(l & 1);
-    // the next layer's inputs go to the other buffer, free since the last barrier
     if (tid == kIssuer && l + 1 < p.n_layers) stage(l + 1);
     const int n_hot = min(Ld.hot_per_slice, n_rows);
     if (!mbar_wait(mbar, (uint32_t)((l >> 1) & 1))) {
       if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
-      mbar_wait(mbar, (uint32_t)((l >> 1) & 1));            // let a copy in flight land
-      if (l + 1 < p.n_layers) mbar_wait(mbar0 + 8u * (uint32_t)((l + 1) & 1), (uint32_t)(((l + 1) >> 1) & 1));
+      drain(l, l + 1);
       return;
     }
     unsigned char *bsm = stage_buf(l & 1);
@@ -338,7 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       __syncthreads();
     }
     PHASE_STAMP(l, 1);
-    if (!grid_barrier(p.bar, ++epoch, status)) return;
+    if (!grid_barrier(p.bar, ++epoch, status)) {
+      drain(l + 1, l + 1);
+      return;
+    }
     PHASE_STAMP(l, 2);
 
     // ---------------- C: logits over my slice, ordered local active list
@@ -352,48 +360,67 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       if (REGLU) rowpf(Ld.R_gate, i);
       rowpf(Ld.R_dT, i);
     }
-    for (int e = tid; e < NB * r; e += kThreads) h_s[e] = ldcg(p.h + e);
+    // h into shared memory as [NB][2][r / 8] float4: elements 0-3 of each
+    // 8-element group in the first half, 4-7 in the second, so that lanes
+    // reading different groups hit distinct banks
+    const int nvr = r >> 3;
+    float4 *h4_s = reinterpret_cast<float4 *>(h_s);
+    for (int e = tid; e < NB * (r >> 2); e += kThreads) {
+      const int t = e / (r >> 2), g4 = e - t * (r >> 2);
+      h4_s[t * 2 * nvr + (g4 & 1) * nvr + (g4 >> 1)] = ldcg(reinterpret_cast<const float4 *>(p.h) + e);
+    }
     __syncthreads();
     PHASE_STAMP(l, 9);
     if (p.staged) {
-      // W_p2 slice in shared memory: one thread per row, vectors visited in
-      // a lane-rotated order so the 16-byte reads of a warp hit distinct banks
-      const int nvr = r >> 3;
-      for (int rl = tid; rl < n_rows; rl += kThreads) {
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(p2_s + (size_t)rl * r);
+      // W_p2 slice in shared memory: 2^lgt_s threads per row, each summing
+      // r / 8 / 2^lgt_s of the row's 16-byte vectors; a row's visiting order
+      // is rotated by its place within the quarter-warp so that the 16-byte
+      // reads of a quarter-warp fall on distinct banks
+      const int lgT = p.lgt_s, T = 1 << lgT;
+      const int nk = nvr >> lgT;                 // vectors per thread
+      const int rpp = kThreads >> lgT;           // rows per pass
+      const int rr = tid >> lgT, sub = tid & (T - 1);
+      const int rot = (rr & ((8 >> lgT) - 1)) % nk;
+      for (int rb = 0; rb < n_rows; rb += rpp) {
+        const int rl = rb + rr;
+        const bool valid = rl < n_rows;
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(p2_s + (size_t)(valid ? rl : 0) * r);
         float a4[NB][4];
 #pragma unroll
         for (int t = 0; t < NB; ++t)
 #pragma unroll
           for (int q = 0; q < 4; ++q) a4[t][q] = 0.f;
-        int vv = lane % nvr;
-        for (int v = 0; v < nvr; ++v) {
-          const uint4 wv = wrow[vv];
+        int kk = rot;
+#pragma unroll 4
+        for (int k = 0; k < nk; ++k) {
+          const int v = sub + (kk << lgT);
+          const uint4 wv = wrow[v];
           const __half2 *wh = reinterpret_cast<const __half2 *>(&wv);
           const float2 w0 = __half22float2(wh[0]), w1 = __half22float2(wh[1]);
           const float2 w2 = __half22float2(wh[2]), w3 = __half22float2(wh[3]);
 #pragma unroll
           for (int t = 0; t < NB; ++t) {
-            const float4 *hp = reinterpret_cast<const float4 *>(h_s + t * r + vv * 8);
-            const float4 h0 = hp[0], h1 = hp[1];
+            const float4 h0 = h4_s[t * 2 * nvr + v], h1 = h4_s[t * 2 * nvr + nvr + v];
             a4[t][0] = fmaf(w0.x, h0.x, fmaf(w0.y, h0.y, a4[t][0]));
             a4[t][1] = fmaf(w1.x, h0.z, fmaf(w1.y, h0.w, a4[t][1]));
             a4[t][2] = fmaf(w2.x, h1.x, fmaf(w2.y, h1.y, a4[t][2]));
             a4[t][3] = fmaf(w3.x, h1.z, fmaf(w3.y, h1.w, a4[t][3]));
           }
-          vv = vv + 1 == nvr ? 0 : vv + 1;
+          kk = kk + 1 == nk ? 0 : kk + 1;
         }
         bool on = false;
 #pragma unroll
-        for (int t = 0; t < NB; ++t)
-          on |= ((a4[t][0] + a4[t][1]) + (a4[t][2] + a4[t][3]) + c_s[s0 + rl - s0a]) > 0.f;
-        flag_s[rl] = on ? 1 : 0;
+        for (int t = 0; t < NB; ++t) {
+          float sl = (a4[t][0] + a4[t][1]) + (a4[t][2] + a4[t][3]);
+          for (int o = T >> 1; o > 0; o >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, o);
+          on |= valid && sl + c_s[s0 + rl - s0a] > 0.f;
+        }
+        if (sub == 0 && valid) flag_s[rl] = on ? 1 : 0;
       }
     } else {
       const int GL = p.lanes_l;                 // lanes per predictor row (8, 16, 32)
       const int rows_per_warp = 32 / GL;
       const int sub = lane % GL;
-      const int nvr = r >> 3;
       const int iters = (n_rows + kWarps * rows_per_warp - 1) / (kWarps * rows_per_warp);
       constexpr int RU = 8;                     // rows in flight per lane
       for (int it0 = 0; it0 < iters; it0 += RU) {
@@ -415,8 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           }
 #pragma unroll
           for (int t = 0; t < NB; ++t) {
-            const float4 *hp = reinterpret_cast<const float4 *>(h_s + t * r + v * 8);
-            const float4 h0 = hp[0], h1 = hp[1];
+            const float4 h0 = h4_s[t * 2 * nvr + v], h1 = h4_s[t * 2 * nvr + nvr + v];
 #pragma unroll
             for (int u = 0; u < RU; ++u) {
               const __half2 *wh = reinterpret_cast<const __half2 *>(&wv[u]);
@@ -698,7 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         }
       }
     PHASE_STAMP(l, 5);
-    if (!grid_barrier(p.bar, ++epoch, status)) return;
+    if (!grid_barrier(p.bar, ++epoch, status)) {
+      drain(l + 1, l + 1);
+      return;
+    }
     PHASE_STAMP(l, 6);
 
     // ---------------- F: y = sum of partials.  Columns (float4) c = cta*8 + j
@@ -757,7 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       }
     }
     PHASE_STAMP(l, 7);
-    if (!grid_barrier(p.bar, ++epoch, status)) return;
+    if (!grid_barrier(p.bar, ++epoch, status)) {
+      drain(l + 1, l + 1);
+      return;
+    }
     PHASE_STAMP(l, 8);
   }
 }
@@ -893,6 +925,11 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   int GL = 32;
   while (GL > 8 && GL * 8 > L0->rank) GL >>= 1;
   p.lanes_l = GL;
+  // staged logits: the most threads per W_p2 row (up to 8, dividing r / 8)
+  // that still cover the slice in one pass of the CTA
+  int lgt = 0;
+  while (lgt < 3 && (step_slice(L0) << (lgt + 1)) <= kThreads && ((L0->rank >> 3) % (2 << lgt)) == 0) ++lgt;
+  p.lgt_s = lgt;
   const int rows_per_neuron = L0->act != PI_ACT_RELU ? 3 : 2;
   // early L2 prefetch of the local active rows: up to ~768 KB of rows per CTA
   const int rb = L0->row_format == PI_ROWS_FP8_E4M3 ? L0->d : 2 * L0->d;   // bytes of a gathered row
