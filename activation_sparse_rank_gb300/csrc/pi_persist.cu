@@ -257,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // layer l's inputs go to buffer l & 1: layer 0's now, layer l + 1's at the
-  // start of layer l (buffer (l + 1) & 1 is free since the last barrier)
+  // layer l's inputs go to buffer l & 1: layer 0's now, layer l + 1's during
+  // layer l's logits (buffer (l + 1) & 1 is free once layer l has begun)
   if (tid == kIssuer) stage(0);
   // on a failed wait: let the stage copies this CTA may have in flight land
   auto drain = [&](int first, int last) {
@@ -271,11 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     PHASE_STAMP(l, 0);
 
     const uint32_t mbar = mbar0 + 8u * (uint32_t)(l & 1);
-    if (tid == kIssuer && l + 1 < p.n_layers) stage(l + 1);
     const int n_hot = min(Ld.hot_per_slice, n_rows);
     if (!mbar_wait(mbar, (uint32_t)((l >> 1) & 1))) {
       if (tid == 0) atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
-      drain(l, l + 1);
+      drain(l, l);
       return;
     }
     unsigned char *bsm = stage_buf(l & 1);
@@ -343,10 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       __syncthreads();
     }
     PHASE_STAMP(l, 1);
-    if (!grid_barrier(p.bar, ++epoch, status)) {
-      drain(l + 1, l + 1);
-      return;
-    }
+    if (!grid_barrier(p.bar, ++epoch, status)) return;   // no copy in flight yet
     PHASE_STAMP(l, 2);
 
     // ---------------- C: logits over my slice, ordered local active list
@@ -371,6 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     }
     __syncthreads();
     PHASE_STAMP(l, 9);
+    // the next layer's inputs go to the other buffer (free since barrier 1):
+    // issued here by the last warp, which has no logits rows to compute when
+    // the slice needs fewer than 16 warps
+    if (tid == kIssuer && l + 1 < p.n_layers) stage(l + 1);
     if (p.staged) {
       // W_p2 slice in shared memory: 2^lgt_s threads per row, each summing
       // r / 8 / 2^lgt_s of the row's 16-byte vectors; a row's visiting order
@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       const int rr = tid >> lgT, sub = tid & (T - 1);
       const int rot = (rr & ((8 >> lgT) - 1)) % nk;
       for (int rb = 0; rb < n_rows; rb += rpp) {
+        if (rb + ((wid * 32) >> lgT) >= n_rows) break;   // no row of this warp in this pass or later
         const int rl = rb + rr;
         const bool valid = rl < n_rows;
         const uint4 *wrow = reinterpret_cast<const uint4 *>(p2_s + (size_t)(valid ? rl : 0) * r);
