@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     PI_ACT_SWIGLU,
     PI_ACT_RELU,
     PI_MAX_BATCH,
+    PI_STACK_LAYERS_PER_LAUNCH,
     Layer,
     PiError,
     hot_first_perm,
@@ -26,6 +27,7 @@ __all__ = [
     "PI_ACT_REGLU",
     "PI_ACT_SWIGLU",
     "PI_MAX_BATCH",
+    "PI_STACK_LAYERS_PER_LAUNCH",
     "hot_first_perm",
     "lib",
     "lib_path",

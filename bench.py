@@ -411,10 +411,13 @@ def main():
         how = "events around each launch, eager step"
     k_ms = [evs[t][0].elapsed_time(evs[t][1]) for t in range(Tr)]
     cnt = stack.count[:Tr].cpu().numpy()
-    if Bt <= 2:   # the persistent step: predictor + rows of every layer
-        alg_bytes = (Tr * n_layers * predictor_bytes(spec.d, spec.ffn, spec.rank)
-                     + float(cnt.sum()) * bytes_per_active_neuron(spec.d, spec.act, rows))
-        kname = f"k_stack_step (one token through {n_layers} layers)"
+    # layers[0]'s timing hook brackets the launch that holds layer 0: the first
+    # PI_STACK_LAYERS_PER_LAUNCH layers of a longer stack
+    L1 = min(n_layers, pi.PI_STACK_LAYERS_PER_LAUNCH)
+    if Bt <= 2:   # the persistent step: predictor + rows of the launch's layers
+        alg_bytes = (Tr * L1 * predictor_bytes(spec.d, spec.ffn, spec.rank)
+                     + float(cnt[:, :L1].sum()) * bytes_per_active_neuron(spec.d, spec.act, rows))
+        kname = f"k_stack_step (one token through {L1} layers)"
     else:         # tensor-core up + down of layer 0: its active rows
         alg_bytes = float(cnt[:, 0].sum()) * bytes_per_active_neuron(spec.d, spec.act)
         kname = "k_tc_rows<act> + k_tc_down (layer 0, tcgen05)"
@@ -424,8 +427,9 @@ def main():
     tfile = ROOT / "profiles" / "stack_step_traffic.json"
     if tfile.exists():
         tj = json.loads(tfile.read_text())
-        if tj.get("kernel_source_hash") == kernel_source_hash():
-            traffic = tj.get("bytes_per_launch")
+        # counters of this kernel on this workload's layers, per layer
+        if tj.get("kernel_source_hash") == kernel_source_hash() and tj.get("config") == cfg.name:
+            traffic = tj["bytes_per_layer"] * L1
     if Bt > 2 or rows != "fp16":     # the stored counters are of the fp16 step kernel
         traffic = None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
