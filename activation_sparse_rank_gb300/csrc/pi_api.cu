@@ -19,6 +19,9 @@ namespace {
 
 thread_local char g_err[512] = "";
 
+// the persistent step takes its whole layer table by value
+static_assert(sizeof(pi::StackParams) <= 4096, "StackParams must fit the classic 4 KB parameter space");
+
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
