@@ -197,6 +197,72 @@ def test_preact_error_bound_covers_binary32():
         assert (np.abs(z32 - z[t]) <= tau[t]).all()
 
 
+def test_logit_error_bound_covers_a_cancelling_hidden_layer():
+    # h = 2^24 + 1 - 2^24 = 1, but a binary32 sum in index order rounds
+    # 2^24 + 1 to 2^24 (ties to even) and returns h = 0; with W_p2 = +-1 and
+    # c_p = -+0.5 both logits change sign.  Only the bound's term for the
+    # error of h (e = gamma_d * sum |W_p1 x|) covers that.
+    f16, f32 = np.float16, np.float32
+    L = O.OracleLayer(act="relu", W_up=np.ones((2, 3), f16), W_gate=None, b=np.zeros(2, f32),
+                      W_down=np.ones((3, 2), f16), W_p1=np.array([[1024, 1, -1024]], f16),
+                      W_p2=np.array([[1], [-1]], f16), c_p=np.array([-0.5, 0.5], f32))
+    x = np.array([[16384, 1, 16384]], f16)
+    h = O.predictor_hidden(L, x)
+    l = O.predictor_logits(L, h)[0]
+    assert h.tolist() == [[1.0]] and l.tolist() == [0.5, -0.5]
+    h32 = np.maximum(0, _fp32_sequential(L.W_p1, x[0].astype(np.float32)))
+    l32 = _fp32_sequential(L.W_p2, h32, bias=L.c_p)
+    assert h32.tolist() == [0.0] and l32.tolist() == [-0.5, 0.5]   # both decisions flip
+    tau = O.logit_error_bound(L, x, h)[0]
+    assert (np.abs(l32 - l) <= tau).all()
+    assert O.predicted_mask(l).tolist() == [True, False]
+
+
+def test_profile_band_counts_only_undecided_pairs():
+    # pre-activations exactly 0, 0 and 7 for the token x = (1, 1): the first
+    # two are inside the binary32 band (either decision is a correct binary32
+    # result), the third is forced; none of them fires in exact arithmetic
+    # except the third
+    f16, f32 = np.float16, np.float32
+    L = O.OracleLayer(act="relu", W_up=np.array([[1, 1], [1, -1], [2, 0]], f16), W_gate=None,
+                      b=np.array([-2, 0, 5], f32), W_down=np.ones((2, 3), f16),
+                      W_p1=np.ones((1, 2), f16), W_p2=np.ones((3, 1), f16), c_p=None)
+    X = np.array([[1, 1], [1, 1], [-1, 2]], f16)      # z = (0, 0, 7), (0, 0, 7), (-1, -3, 3)
+    counts, band = O.profile_counts(L, X)
+    assert counts.tolist() == [0, 0, 3]
+    assert band.tolist() == [2, 2, 0]
+
+
+def test_preact_error_bound_covers_a_bias_dominated_sum():
+    # z = 2^-12 * 2^-13 + 1 = 1 + 2^-25: binary32 rounds the last addition
+    # to 1, an error of 2^-25 that only the bound's |b| term covers
+    f16, f32 = np.float16, np.float32
+    L = O.OracleLayer(act="relu", W_up=np.array([[2.0 ** -12]], f16), W_gate=None,
+                      b=np.array([1.0], f32), W_down=np.ones((1, 1), f16),
+                      W_p1=np.ones((1, 1), f16), W_p2=np.ones((1, 1), f16), c_p=None)
+    x = np.array([[2.0 ** -13]], f16)
+    _, z = O.exact_mask(L, x)
+    z32 = _fp32_sequential(L.W_up, x[0].astype(np.float32), bias=L.b)
+    assert z[0, 0] == 1.0 + 2.0 ** -25 and z32[0] == np.float32(1.0)
+    assert abs(float(z32[0]) - z[0, 0]) <= O.preact_error_bound(L, x)[0, 0]
+
+
+def test_activations_and_sum_follow_the_order_of_s():
+    # the operators take S in any order: a[:, k] belongs to neuron S[k] and
+    # pairs with W_down[:, S[k]]
+    spec = LayerSpec(d=64, ffn=200, rank=8, act="reglu", mean_f=0.3)
+    L = O.OracleLayer.from_tensors(make_layer(spec, 31))
+    x = make_tokens(64, 2, seed=32).numpy()
+    S = np.arange(0, 200, 3)
+    perm = np.random.default_rng(5).permutation(S.size)
+    a = O.ffn_activations(L, x, S)
+    a_p = O.ffn_activations(L, x, S[perm])
+    assert np.array_equal(a_p, a[:, perm])
+    y = O.ffn_output(L, S, a)
+    y_p = O.ffn_output(L, S[perm], a_p)
+    assert np.allclose(y_p, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
 def test_firing_rate_construction():
     f, c = firing_rates(4096, 1.0, 0.10, 0.9, seed=3)
     assert abs(f.mean() - 0.10) < 1e-9
