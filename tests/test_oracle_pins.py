@@ -288,6 +288,37 @@ def test_generator_fires_at_target_rates():
     assert abs(counts.sum() / (T * 4096) - 0.10) < 0.005
 
 
+@pytest.mark.parametrize("act", ["relu", "reglu", "swiglu"])
+def test_bias_gives_each_neuron_its_target_firing_probability(act):
+    # for x ~ N(0, I) the gated pre-activation of neuron i is normal with
+    # standard deviation ||W_i|| (the gate's row for gated layers), so it is
+    # positive with probability Phi(b_i / ||W_i||), which must be f_i
+    from scipy.stats import norm
+    spec = LayerSpec(d=256, ffn=1024, rank=16, act=act, mean_f=0.15)
+    t = make_layer(spec, 29)
+    W = (t["W_gate"] if act != "relu" else t["W_up"]).double().numpy()
+    p = norm.cdf(t["b"].double().numpy() / np.linalg.norm(W, axis=1))
+    assert np.abs(p - t["f"].numpy()).max() < 1e-6
+
+
+def test_predictor_logit_moments_match_monte_carlo():
+    # mean and variance of W_p2_i . ReLU(W_p1 x) over x ~ N(0, I), which set
+    # the calibrated c_p, against 400k sampled tokens (6 standard errors)
+    from workload.gen import predictor_logit_moments
+    g = np.random.default_rng(41)
+    W_p1 = g.normal(0, 0.3, (6, 16)).astype(np.float16)
+    W_p2 = g.normal(0, 0.3, (5, 6)).astype(np.float16)
+    mu, var = (m.numpy() for m in predictor_logit_moments(torch.from_numpy(W_p1), torch.from_numpy(W_p2)))
+    N = 400_000
+    x = g.standard_normal((N, 16))
+    l0 = np.maximum(0.0, x @ W_p1.astype(np.float64).T) @ W_p2.astype(np.float64).T
+    m_hat, v_hat = l0.mean(axis=0), l0.var(axis=0)
+    se_m = np.sqrt(v_hat / N)
+    se_v = np.sqrt(((l0 - m_hat) ** 4).mean(axis=0) / N)
+    assert (np.abs(m_hat - mu) <= 6 * se_m).all()
+    assert (np.abs(v_hat - var) <= 6 * se_v).all()
+
+
 def test_calibrated_predictor_density():
     spec = LayerSpec(d=1024, ffn=4096, rank=64, mean_f=0.10)
     t = make_layer(spec, 23)

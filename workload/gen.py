@@ -85,8 +85,9 @@ def _row_norms(W: torch.Tensor, chunk: int = 4096) -> torch.Tensor:
     return out
 
 
-def _calibrated_predictor_bias(W_p1: torch.Tensor, W_p2: torch.Tensor,
-                               f: torch.Tensor) -> torch.Tensor:
+def predictor_logit_moments(W_p1: torch.Tensor, W_p2: torch.Tensor):
+    """Mean and variance of W_p2_i . h over x ~ N(0, I), h = ReLU(W_p1 x),
+    from the first- and second-order arc-cosine moments of ReLU features."""
     A = W_p1.double()
     s = A.pow(2).sum(1).sqrt()                                  # [r]
     G = A @ A.T
@@ -101,6 +102,12 @@ def _calibrated_predictor_bias(W_p1: torch.Tensor, W_p2: torch.Tensor,
         B = W_p2[i:i + 8192].double()
         mu[i:i + 8192] = B @ E_h
         var[i:i + 8192] = ((B @ C) * B).sum(1)
+    return mu, var
+
+
+def _calibrated_predictor_bias(W_p1: torch.Tensor, W_p2: torch.Tensor,
+                               f: torch.Tensor) -> torch.Tensor:
+    mu, var = predictor_logit_moments(W_p1, W_p2)
     return (-mu + var.clamp_min(0).sqrt() * _ndtri(f)).float()
 
 
