@@ -86,3 +86,19 @@ def test_binding_constants_match_the_header(pi):
     enums = dict(re.findall(r"\b(PI_(?:ACT|ROWS)_[A-Z0-9_]+)\s*=\s*([0-9]+)", text))
     for name, value in enums.items():
         assert getattr(pi.binding, name) == int(value), name
+
+
+def test_binding_checks_arguments_before_the_library(pi):
+    # argument marshalling refuses host tensors, wrong dtypes and unknown
+    # activations before any pointer reaches the C ABI
+    import torch
+    W = torch.zeros(8, 8, dtype=torch.float16)
+    b = torch.zeros(8)
+    with pytest.raises(ValueError):
+        pi.binding.make_desc(W, None, b, W, W, W, None, "gelu")
+    with pytest.raises(TypeError):
+        pi.binding.make_desc(W, None, b, W, W, W, None, "relu")       # host memory
+    with pytest.raises(TypeError):
+        pi.Layer.from_dict(dict(W_up=W, W_gate=None, b=b, W_down=W, W_p1=W, W_p2=W,
+                                c_p=None, act="relu"))
+
