@@ -60,6 +60,7 @@ _SIG = {
     "pi_ffn_dense_ref": (C.c_int, [_p, _p, _i32, _p, _p, C.c_size_t, _p]),
     "pi_layer_forward": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
     "pi_stack_forward": (C.c_int, [_p, _i32, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
+    "pi_stack_forward_chained": (C.c_int, [_p, _i32, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
     "pi_profile_activations": (C.c_int, [C.POINTER(pi_layer_desc), _p, _i32, _p, _p]),
     "pi_hot_first_perm": (C.c_int, [_p, _i32, _p]),
     "pi_device_status": (C.c_int, [_p, _p]),
@@ -277,8 +278,11 @@ class Layer:
         return int(lib.pi_device_status(self._h, _stream(stream)))
 
 
-def stack_forward(layers, x, y, idx=None, count=None, ws=None, stream=None, handles=None):
+def stack_forward(layers, x, y, idx=None, count=None, ws=None, stream=None, handles=None,
+                  chained=False):
     """Run layers in order on x [n_layers, B, d] fp16 into y [n_layers, B, d] fp32.
+    chained: only x[0] is an input; x[l] for l >= 1 is overwritten with
+    fp16(y[l-1] / RMS(y[l-1])) before layer l runs (pi_stack_forward_chained).
     `handles` may carry a prebuilt ctypes array of the layer handles."""
     n = len(layers)
     _req(x, torch.float16, "x")
@@ -287,8 +291,10 @@ def stack_forward(layers, x, y, idx=None, count=None, ws=None, stream=None, hand
         handles = (C.c_void_p * n)(*[l.handle.value for l in layers])
     if ws is None:
         ws = layers[0].workspace(B)
-    _check(lib.pi_stack_forward(handles, n, _ptr(x), B, _ptr(idx), _ptr(count), _ptr(y),
-                                _ptr(ws), ws.numel(), _stream(stream)), "pi_stack_forward")
+    fn, name = ((lib.pi_stack_forward_chained, "pi_stack_forward_chained") if chained
+                else (lib.pi_stack_forward, "pi_stack_forward"))
+    _check(fn(handles, n, _ptr(x), B, _ptr(idx), _ptr(count), _ptr(y), _ptr(ws), ws.numel(),
+              _stream(stream)), name)
     return y
 
 

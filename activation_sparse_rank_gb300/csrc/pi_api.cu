@@ -570,10 +570,31 @@ pi_status pi_layer_forward(pi_layer *L, const uint16_t *x, int32_t B, int32_t *i
   return PI_OK;
 }
 
-pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint16_t *x,
-                           int32_t B, int32_t *idx, int32_t *count, float *y, void *ws,
-                           size_t ws_bytes, void *stream) {
-  g_err[0] = 0;
+}  // extern "C"
+
+namespace {
+
+// Chained input of the next layer: x[t] = fp16(y[t] / RMS(y[t])) with
+// RMS(v) = sqrt(mean(v^2) + 1e-12), binary32, one CTA per token.
+__global__ void __launch_bounds__(256) k_chain_x(const float *__restrict__ y, __half *__restrict__ x, int d) {
+  __shared__ float red[8];
+  const float *yt = y + (size_t)blockIdx.x * d;
+  float s = 0.f;
+  for (int j = threadIdx.x; j < d; j += 256) s = fmaf(yt[j], yt[j], s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)d + 1e-12f);
+  for (int j = threadIdx.x; j < d; j += 256) x[(size_t)blockIdx.x * d + j] = __float2half_rn(yt[j] * inv);
+}
+
+pi_status stack_forward_impl(pi_layer *const *layers, int32_t n_layers, uint16_t *x_mut,
+                             const uint16_t *x, int32_t B, int32_t *idx, int32_t *count, float *y,
+                             void *ws, size_t ws_bytes, void *stream, bool chained,
+                             const char *where) {
   if (!layers || n_layers < 1) return pi::fail(PI_ERR_INVALID_ARG, "layers is NULL or n_layers < 1");
   for (int l = 0; l < n_layers; ++l) {
     const pi_layer *Ll = layers[l];
@@ -596,15 +617,19 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *wsb = static_cast<char *>(ws);
   const __half *xh = reinterpret_cast<const __half *>(x);
+  __half *xm = reinterpret_cast<__half *>(x_mut);
   const size_t xs = (size_t)B * L->d;
   if (B <= 2) {
     for (int l0 = 0; l0 < n_layers; l0 += pi::kMaxStack) {
       const int n = std::min(pi::kMaxStack, n_layers - l0);
+      __half *x_next = chained && l0 + n < n_layers ? xm + (l0 + n) * xs : nullptr;
       PI_TRY_CUDA(pi::run_stack(layers + l0, n, xh + l0 * xs, B, idx ? idx + (size_t)l0 * L->ffn : nullptr,
-                                count ? count + l0 : nullptr, y + l0 * xs, w, wsb, s));
+                                count ? count + l0 : nullptr, y + l0 * xs, w, wsb, s, chained,
+                                chained ? xm + l0 * xs : nullptr, x_next));
     }
     return PI_OK;
-  }  st = need_fp16_rows(L, "pi_stack_forward with more than 2 tokens");
+  }
+  st = need_fp16_rows(L, where);
   if (st != PI_OK) return st;
 
   for (int l = 0; l < n_layers; ++l) {
@@ -621,8 +646,32 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
     }
     PI_TRY_CUDA(pi::run_sparse_ffn(Ll, xh + l * xs, B, idx + (size_t)l * L->ffn, count + l, 0,
                                    y + l * xs, w, wsb, s));
+    if (chained && l + 1 < n_layers) {
+      k_chain_x<<<B, 256, 0, s>>>(y + l * xs, xm + (l + 1) * xs, L->d);
+      PI_TRY_CUDA(cudaGetLastError());
+    }
   }
   return PI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint16_t *x,
+                           int32_t B, int32_t *idx, int32_t *count, float *y, void *ws,
+                           size_t ws_bytes, void *stream) {
+  g_err[0] = 0;
+  return stack_forward_impl(layers, n_layers, nullptr, x, B, idx, count, y, ws, ws_bytes, stream,
+                            false, "pi_stack_forward with more than 2 tokens");
+}
+
+pi_status pi_stack_forward_chained(pi_layer *const *layers, int32_t n_layers, uint16_t *x,
+                                   int32_t B, int32_t *idx, int32_t *count, float *y, void *ws,
+                                   size_t ws_bytes, void *stream) {
+  g_err[0] = 0;
+  return stack_forward_impl(layers, n_layers, x, x, B, idx, count, y, ws, ws_bytes, stream, true,
+                            "pi_stack_forward_chained with more than 2 tokens");
 }
 
 pi_status pi_profile_activations(const pi_layer_desc *D, const uint16_t *x, int32_t T,

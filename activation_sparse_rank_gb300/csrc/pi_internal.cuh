@@ -85,12 +85,15 @@ struct LayerDev {
 struct StackParams {
   int n_layers, d, ffn, rank;
   int G, staged, lanes_l, pf_rows, pf_next;
+  int chained;                   // x of layer l > 0 formed from y of layer l - 1
   int lgt_s;                     // log2 threads per staged W_p2 row (logits)
   int off_flag, off_list, off_lb, off_a, off_stage, stage_bytes, slice_pad;   // shared memory layout
   int soff_c, soff_b, soff_p1, soff_p2;                     // offsets inside a stage buffer
   int soff_su, soff_sg, soff_sd;                            // row-scale slices (FP8 layers)
   int gate_silu;                                            // gated layers: SiLU gate (SwiGLU)
-  const __half *x;       // [n_layers, B, d]
+  const __half *x;       // [n_layers, B, d] (chained: only layer 0 is read)
+  __half *x_out;         // chained: [n_layers, B, d], the inputs formed (layer 0 untouched); else nullptr
+  __half *x_next;        // chained: [B, d], the input of the layer after this launch, or nullptr
   float *y;              // [n_layers, B, d]
   int32_t *count;        // [n_layers] or nullptr
   uint8_t *mask_out;     // [n_layers, ffn] union masks (for the idx output) or nullptr
@@ -108,8 +111,11 @@ size_t step_smem(const pi_layer *L, int B);
 // Ascending active lists of n layers from their union masks [n, ffn] (one CTA per layer).
 cudaError_t run_compact_layers(const pi_layer *L, const uint8_t *masks, int n, int32_t *idx,
                                int32_t *count, cudaStream_t s);
+// chained: x of layer l > 0 is fp16(y_{l-1} / RMS(y_{l-1})), written to x_out
+// [n, B, d]; x_next (or nullptr) receives the input of the layer after layer n - 1.
 cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, int32_t *idx,
-                      int32_t *count, float *y, const WsLayout &w, char *ws, cudaStream_t s);
+                      int32_t *count, float *y, const WsLayout &w, char *ws, cudaStream_t s,
+                      bool chained = false, __half *x_out = nullptr, __half *x_next = nullptr);
 WsLayout ws_layout(const pi_layer *L, int B);
 int fused_splits(const pi_layer *L);        // CTAs of the batch-1 fused kernel
 int down_splits(const pi_layer *L, int B);  // split count of the generic down kernel

@@ -19,6 +19,9 @@
 //   -- barrier 2 (partials complete)
 //   F  y = sum of the G partials in a fixed order (deterministic)
 //   -- barrier 3 (y complete: the next layer may depend on it, as in decode)
+// In chained mode the next layer's input is formed from y on the device,
+// x_{l+1} = fp16(y_l / RMS(y_l)), after barrier 3 (nothing of x_{l+1} is
+// read earlier).
 //
 // Grid barriers are a release-add on a global counter and an acquire poll
 // with an iteration cap; mbarrier waits are capped too.  On a cap the kernel
@@ -130,13 +133,14 @@ __device__ unsigned long long g_cta_e[160][16][2];
 #endif
 
 // Stage the inputs of one layer for this CTA into shared memory (one thread,
-// TMA bulk copies completing on `mbar`): the token rows x [NB, d], the CTA's
+// TMA bulk copies completing on `mbar`): the token rows x [NB, d] (unless
+// with_x is false), the CTA's
 // slices of c_p and b (from the 16-byte boundary at or below s0; the layer
 // allocation pads both vectors to 256 bytes, so the rounded-up end stays
 // inside it) and, when `with_pred`, its W_p1 rows k = cta, cta+G, ... and
 // its W_p2 slice.
-__device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half *x, int nb, int cta,
-                                            int G, int d, int r, int s0, int s1, bool with_pred,
+__device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half *x, int nb, bool with_x,
+                                            int cta, int G, int d, int r, int s0, int s1, bool with_pred,
                                             __half *x_s, float *c_s, float *b_s, __half *p1_s,
                                             __half *p2_s, float *su_s, float *sg_s, float *sd_s,
                                             uint32_t mbar) {
@@ -144,7 +148,7 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
   // ReGLU, down^T), or nullptr
   const int s0a = s0 & ~3;
   const uint32_t cb_bytes = (uint32_t)(((s1 - s0a) + 3) & ~3) * 4u;
-  const uint32_t x_bytes = (uint32_t)nb * (uint32_t)d * 2u;
+  const uint32_t x_bytes = with_x ? (uint32_t)nb * (uint32_t)d * 2u : 0u;
   const uint32_t row_bytes = (uint32_t)d * 2u;
   const uint32_t p2_bytes = with_pred ? (uint32_t)(s1 - s0) * (uint32_t)r * 2u : 0u;
   int na = 0;
@@ -153,7 +157,7 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
   const uint32_t nsc = su_s ? (sg_s ? 3u : 2u) : 0u;
   const uint32_t total = x_bytes + (cb_bytes ? (2u + nsc) * cb_bytes : 0u) + (uint32_t)na * row_bytes + p2_bytes;
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(total) : "memory");
-  tma_load_1d(x_s, x, x_bytes, mbar);
+  if (x_bytes) tma_load_1d(x_s, x, x_bytes, mbar);
   if (cb_bytes) {
     tma_load_1d(c_s, Ld.c_p + s0a, cb_bytes, mbar);
     tma_load_1d(b_s, Ld.b + s0a, cb_bytes, mbar);
@@ -205,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   const uint32_t row_bytes = (uint32_t)d * 2u;                 // an fp16 row (predictor)
   const uint32_t rrow = FP8 ? (uint32_t)d : row_bytes;          // a gathered up / gate / down row
   unsigned *status = p.status;
+  const bool chained = p.chained != 0;
+  __shared__ float ss_s[kWarps][NB];
   // 8-element vector v of gathered row i of R (fp16 or E4M3 codes)
   auto ldrow = [&](const void *R, int i, int v) -> RowVec {
     const char *row = static_cast<const char *>(R) + (size_t)i * rrow;
@@ -242,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   const int s0a = s0 & ~3;                       // c / b slices start at this neuron
   auto stage = [&](int layer) {                  // one thread: issue layer's inputs into its buffer
     unsigned char *bsm = stage_buf(layer & 1);
-    stage_layer(p.layers[layer], p.x + (size_t)layer * NB * d, NB, cta, G, d, r, s0, s1,
-                p.staged != 0, reinterpret_cast<__half *>(bsm), reinterpret_cast<float *>(bsm + p.soff_c),
+    stage_layer(p.layers[layer], p.x + (size_t)layer * NB * d, NB, !chained || layer == 0, cta, G, d, r,
+                s0, s1, p.staged != 0, reinterpret_cast<__half *>(bsm), reinterpret_cast<float *>(bsm + p.soff_c),
                 reinterpret_cast<float *>(bsm + p.soff_b), reinterpret_cast<__half *>(bsm + p.soff_p1),
                 reinterpret_cast<__half *>(bsm + p.soff_p2),
                 FP8 ? reinterpret_cast<float *>(bsm + p.soff_su) : nullptr,
@@ -288,26 +294,72 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     const __half *p1_s = reinterpret_cast<const __half *>(bsm + p.soff_p1);
     const __half *p2_s = reinterpret_cast<const __half *>(bsm + p.soff_p2);
     uint4 xr[NB][CPT];
+    if (chained && l > 0) {
+      // x = fp16(y / RMS(y)) of the previous layer's y, complete since
+      // barrier 3 (every CTA forms the whole vector in the same order, so all
+      // agree bit for bit)
+      const float *yp = p.y + (size_t)(l - 1) * NB * d;
+      float yv[NB][CPT][8];
 #pragma unroll
-    for (int t = 0; t < NB; ++t)
+      for (int t = 0; t < NB; ++t) {
+        float ss = 0.f;
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) {
-        const int v = tid + c * kThreads;
-        xr[t][c] = v < nv ? reinterpret_cast<const uint4 *>(x_s + (size_t)t * d)[v]
-                          : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < CPT; ++c) {
+          const int v = tid + c * kThreads;
+          float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+          if (v < nv) {
+            a0 = ldcg(reinterpret_cast<const float4 *>(yp + (size_t)t * d) + 2 * v);
+            a1 = ldcg(reinterpret_cast<const float4 *>(yp + (size_t)t * d) + 2 * v + 1);
+          }
+          yv[t][c][0] = a0.x; yv[t][c][1] = a0.y; yv[t][c][2] = a0.z; yv[t][c][3] = a0.w;
+          yv[t][c][4] = a1.x; yv[t][c][5] = a1.y; yv[t][c][6] = a1.z; yv[t][c][7] = a1.w;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) ss = fmaf(yv[t][c][k], yv[t][c][k], ss);
+        }
+        ss = pidev::warp_sum(ss);
+        if (lane == 0) ss_s[wid][t] = ss;
       }
-
-    // ---------------- A: h = ReLU(W_p1 x), rows cta, cta + G, ... (8 rows per pass)
-    for (int q0 = 0; cta + q0 * G < r; q0 += 8) {
-      float hs[8][NB];
+      __syncthreads();
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int t = 0; t < NB; ++t) {
+        float sum = 0.f;
+        for (int w2 = 0; w2 < kWarps; ++w2) sum += ss_s[w2][t];
+        const float inv = 1.0f / sqrtf(sum / (float)d + 1e-12f);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          __half2 hv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            hv[k] = __floats2half2_rn(yv[t][c][2 * k] * inv, yv[t][c][2 * k + 1] * inv);
+          xr[t][c] = *reinterpret_cast<const uint4 *>(hv);
+          const int v = tid + c * kThreads;
+          if (cta == 0 && v < nv)           // the input this layer used, for the caller
+            reinterpret_cast<uint4 *>(p.x_out + ((size_t)l * NB + t) * d)[v] = xr[t][c];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < NB; ++t)
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          const int v = tid + c * kThreads;
+          xr[t][c] = v < nv ? reinterpret_cast<const uint4 *>(x_s + (size_t)t * d)[v]
+                            : make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // ---------------- A: h = ReLU(W_p1 x), rows cta, cta + G, ... (2 rows per pass)
+    for (int q0 = 0; cta + q0 * G < r; q0 += 2) {
+      const bool two = cta + (q0 + 1) * G < r;   // uniform over the CTA
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (q == 1 && !two) break;
         const int k = cta + (q0 + q) * G;
         uint4 w[CPT];
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
           const int v = tid + c * kThreads;
-          if (k < r && v < nv)
+          if (v < nv)
             w[c] = p.staged ? reinterpret_cast<const uint4 *>(p1_s + (size_t)(q0 + q) * d)[v]
                             : pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p1 + (size_t)k * d) + v);
           else
@@ -315,28 +367,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         }
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
-          float s = 0.f;
+          float sum = 0.f;
 #pragma unroll
-          for (int c = 0; c < CPT; ++c) s = pidev::dot8(s, w[c], xr[t][c]);
-          hs[q][t] = s;
+          for (int c = 0; c < CPT; ++c) sum = pidev::dot8(sum, w[c], xr[t][c]);
+          sum = pidev::warp_sum(sum);
+          if (lane == 0) ared_s[wid][t][q] = sum;
         }
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (cta + (q0 + q) * G < r)              // uniform over the CTA
-#pragma unroll
-          for (int t = 0; t < NB; ++t) {
-            const float s = pidev::warp_sum(hs[q][t]);
-            if (lane == 0) ared_s[wid][t][q] = s;
-          }
       __syncthreads();
-      if (tid < 8 * NB) {
+      if (tid < 2 * NB) {
         const int q = tid / NB, t = tid % NB;
         const int k = cta + (q0 + q) * G;
         if (k < r) {
-          float s = 0.f;
-          for (int w2 = 0; w2 < kWarps; ++w2) s += ared_s[w2][t][q];
-          p.h[(size_t)t * r + k] = s > 0.f ? s : 0.f;
+          float sum = 0.f;
+          for (int w2 = 0; w2 < kWarps; ++w2) sum += ared_s[w2][t][q];
+          p.h[(size_t)t * r + k] = sum > 0.f ? sum : 0.f;
         }
       }
       __syncthreads();
@@ -756,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         const int c = c0 + j;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c < n4) {
-          constexpr int kPR = 8;
+          constexpr int kPR = 4;
           for (int sp0 = g; sp0 < G; sp0 += 64 * kPR) {
             float4 v[kPR];
 #pragma unroll
@@ -792,6 +837,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       return;
     }
     PHASE_STAMP(l, 8);
+  }
+  // chained across launches: the input of the layer after this launch
+  if (chained && p.x_next && cta == 0 && p.n_layers > 0) {
+    const float *yp = p.y + (size_t)(p.n_layers - 1) * NB * d;
+#pragma unroll
+    for (int t = 0; t < NB; ++t) {
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        const int v = tid + c * kThreads;
+        if (v < nv)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float yk = ldcg(yp + (size_t)t * d + 8 * v + k);
+            ss = fmaf(yk, yk, ss);
+          }
+      }
+      ss = pidev::warp_sum(ss);
+      if (lane == 0) ss_s[wid][t] = ss;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < NB; ++t) {
+      float sum = 0.f;
+      for (int w2 = 0; w2 < kWarps; ++w2) sum += ss_s[w2][t];
+      const float inv = 1.0f / sqrtf(sum / (float)d + 1e-12f);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        const int v = tid + c * kThreads;
+        if (v < nv) {
+          __half2 hv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            hv[k] = __floats2half2_rn(ldcg(yp + (size_t)t * d + 8 * v + 2 * k) * inv,
+                                      ldcg(yp + (size_t)t * d + 8 * v + 2 * k + 1) * inv);
+          reinterpret_cast<uint4 *>(p.x_next + (size_t)t * d)[v] = *reinterpret_cast<const uint4 *>(hv);
+        }
+      }
+    }
   }
 }
 
@@ -899,7 +983,8 @@ size_t step_smem(const pi_layer *L, int B) {
 }
 
 cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, int32_t *idx,
-                      int32_t *count, float *y, const WsLayout &w, char *ws, cudaStream_t s) {
+                      int32_t *count, float *y, const WsLayout &w, char *ws, cudaStream_t s,
+                      bool chained, __half *x_out, __half *x_next) {
   const pi_layer *L0 = layers[0];
   const SmemPlan sp = smem_plan(L0, B);
   StackParams p = {};
@@ -938,7 +1023,10 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   p.pf_rows = pf < 1 ? 1 : pf;
   const size_t pred_bytes = 2ull * L0->rank * L0->d + 2ull * L0->ffn * L0->rank;
   p.pf_next = pred_bytes <= (32ull << 20);
+  p.chained = chained ? 1 : 0;
   p.x = x;
+  p.x_out = chained ? x_out : nullptr;
+  p.x_next = chained ? x_next : nullptr;
   p.y = y;
   p.count = count;
   p.mask_out = idx ? reinterpret_cast<uint8_t *>(ws + w.mask) : nullptr;

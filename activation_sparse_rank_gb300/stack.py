@@ -18,7 +18,8 @@ from .binding import PI_STACK_LAYERS_PER_LAUNCH, Layer, stack_forward
 
 
 class SparseFFNStack:
-    def __init__(self, layers: List[Layer], tokens: int, B: int = 1, want_idx: bool = False):
+    def __init__(self, layers: List[Layer], tokens: int, B: int = 1, want_idx: bool = False,
+                 chained: bool = False):
         if not layers:
             raise ValueError("empty stack")
         self.layers = layers
@@ -40,6 +41,9 @@ class SparseFFNStack:
         self.handles = (C.c_void_p * self.L)(*[l.handle.value for l in layers])
         self.graph: Optional[torch.cuda.CUDAGraph] = None
         self.stream = torch.cuda.Stream(device=dev)
+        # chained: each token's layer l >= 1 takes fp16(y_{l-1} / RMS(y_{l-1}))
+        # as its input (formed on the device); only x[t, 0] is read
+        self.chained = bool(chained)
 
     def launches_per_step(self) -> int:
         """Kernels of this library launched per step (memsets not counted)."""
@@ -50,7 +54,7 @@ class SparseFFNStack:
 
     def _token(self, t: int, stream):
         stack_forward(self.layers, self.x[t], self.y[t], idx=self.idx, count=self.count[t],
-                      ws=self.ws, stream=stream, handles=self.handles)
+                      ws=self.ws, stream=stream, handles=self.handles, chained=self.chained)
 
     def enqueue(self, stream=None, tokens=None):
         """Enqueue the step (all tokens, all layers) on `stream` without a graph."""

@@ -36,6 +36,10 @@ from workload import config_by_name, make_layer, make_tokens, sub_seed  # noqa: 
 
 METRIC = "sparse-FFN tokens/s at batch 1; effective HBM GB/s on touched bytes vs peak"
 NOMINAL_HBM_GBS = 8000.0
+# neurons active on more than this share of the profiled tokens are "hot": the
+# step kernel loads the rows of each slice's leading hot places before its
+# predictor has decided
+HOT_FRAC = 0.5
 
 
 def parse():
@@ -53,6 +57,11 @@ def parse():
                     help="storage of the gathered up/gate/down rows (fp8: E4M3 codes, per-row scale)")
     ap.add_argument("--batch", type=int, default=1,
                     help="tokens per decode batch (the headline metric is batch 1)")
+    ap.add_argument("--chained", action="store_true",
+                    help="time the chained decode step as the main line (x of layer l+1 = "
+                         "fp16(y_l / RMS(y_l)) formed on the device)")
+    ap.add_argument("--no-chained-line", action="store_true",
+                    help="skip the chained-decode figure reported beside the main line")
     return ap.parse_args()
 
 
@@ -132,7 +141,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
-def build_stack(cfg, device, n_layers, keep_host_layers, rows="fp16"):
+def build_stack(cfg, device, n_layers, keep_host_layers, rows="fp16", hot_frac=HOT_FRAC):
     import activation_sparse_rank_gb300 as pi
     spec = cfg.layer
     layers, host_layers = [], []
@@ -144,8 +153,8 @@ def build_stack(cfg, device, n_layers, keep_host_layers, rows="fp16"):
             Xp = make_tokens(spec.d, cfg.profile_tokens, sub_seed(cfg.seed, l, "profile"), device)
             counts = pi.profile_activations(t, Xp).cpu().numpy()
             perm = pi.hot_first_perm(counts)
-            # hot: active on more than half of the profiled tokens
-            n_hot = int((counts > cfg.profile_tokens // 2).sum())
+            # hot: active on more than hot_frac of the profiled tokens
+            n_hot = int((counts > hot_frac * cfg.profile_tokens).sum())
             del Xp
         layer = pi.Layer.from_dict(t, perm=perm, rows=rows)
         layer.set_hot_count(n_hot)
@@ -246,7 +255,8 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(cfg, n_layers: int, T: int, Bt: int, world: int, rows: str = "fp16") -> dict:
+def workload_config(cfg, n_layers: int, T: int, Bt: int, world: int, rows: str = "fp16",
+                    chained: bool = False) -> dict:
     """The config object both arms print for one workload."""
     spec = cfg.layer
     weights = "fp16" if rows == "fp16" else "fp16 predictor; up/gate/down rows FP8 E4M3 with a per-row fp32 scale"
@@ -254,7 +264,10 @@ def workload_config(cfg, n_layers: int, T: int, Bt: int, world: int, rows: str =
             "rank": spec.rank, "layers": n_layers, "tokens_per_step": T * Bt, "batch": Bt,
             "act": spec.act, "weights": weights, "hot_first": bool(cfg.profile_tokens),
             "l2": "inputs larger than L2: the distinct weight rows of a step exceed the 129 MB L2",
-            "parallelism": f"replicas{world}"}
+            "parallelism": f"replicas{world}",
+            "inputs": ("chained: x of layer l+1 = fp16(y_l / RMS(y_l)) on the device" if chained
+                       else "independent seeded x ~ N(0, I) per (token, layer); layer l+1 starts "
+                            "only after layer l's y is complete")}
 
 
 def max_over_ranks(value: float, device=None) -> float:
@@ -308,7 +321,7 @@ def main():
     t_setup = time.perf_counter()
     layers, host_layers = build_stack(cfg, device, n_layers, keep_host_layers=2 if want_cpu else 0,
                                       rows=rows)
-    stack = SparseFFNStack(layers, tokens=T, B=Bt)
+    stack = SparseFFNStack(layers, tokens=T, B=Bt, chained=args.chained)
     X = make_tokens(spec.d, T * n_layers * Bt, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
     stack.x.copy_(X.view(T, n_layers, Bt, spec.d))
     del X
@@ -464,6 +477,35 @@ def main():
            "h2d_bytes_per_step": xh.numel() * xh.element_size(),
            "d2h_bytes_per_step": yh.numel() * yh.element_size()}
 
+    # the same step with each layer's input formed from the previous layer's
+    # output on the device (a decoder's dependence), beside the main line
+    chained_line = None
+    if not args.chained and not args.no_chained_line:
+        cst = SparseFFNStack(layers, tokens=T, B=Bt, chained=True)
+        cst.x[:, 0].copy_(stack.x[:, 0])
+        cst.build_graph()
+        for _ in range(2):
+            with torch.cuda.stream(cst.stream):
+                cst.graph.replay()
+        cst.stream.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        Kc = max(3, min(args.steps, 5))
+        c0.record(cst.stream)
+        with torch.cuda.stream(cst.stream):
+            for _ in range(Kc):
+                cst.graph.replay()
+        c1.record(cst.stream)
+        cst.stream.synchronize()
+        c_ms = c0.elapsed_time(c1) / Kc
+        c_tb = touched_bytes(cfg, cst.count, rows)
+        chained_line = {"value": tokens_step * world / (c_ms / 1000.0), "unit": "tokens/s",
+                        "ms_per_step": c_ms, "effective_hbm_gbs": c_tb / (c_ms / 1000.0) / 1e9,
+                        "mean_active": float(cst.count.double().mean().item()),
+                        "what": "x of layer l+1 = fp16(y_l / RMS(y_l)) formed on the device after "
+                                "layer l completes; only layer 0's x is an input"}
+        del cst
+
     cpu = None
     if want_cpu:
         xh_l = stack.x[:, :2].cpu()
@@ -477,7 +519,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": workload_config(cfg, n_layers, T, Bt, world, rows),
+            "config": workload_config(cfg, n_layers, T, Bt, world, rows, args.chained),
             "effective_hbm_gbs": eff_gbs,
             "effective_frac_of_measured": eff_gbs / peak,
             "effective_frac_of_nominal_8tbs": eff_gbs / (NOMINAL_HBM_GBS),
@@ -485,6 +527,7 @@ def main():
             "dense_tokens_per_s": dense_tok_s,
             "speedup_vs_dense": value / world / dense_tok_s if dense_tok_s else None,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "chained_decode": chained_line,
             "gpu_launches": gpu_launches, "clocks": clk, "setup_s": setup_s,
         }
         print(json.dumps(line), flush=True)

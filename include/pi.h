@@ -223,15 +223,31 @@ pi_status pi_layer_forward(pi_layer *layer, const uint16_t *x, int32_t B,
  *   count   device int32 [n_layers] active counts, or NULL (B <= 2 only)
  *   y       device fp32 [n_layers, B, d]
  *   ws      workspace of pi_workspace_bytes(layers[0], B) bytes
- * For B <= 2 each group of up to 64 layers is one cooperative launch with one
- * CTA per SM and four grid-wide barriers per layer (predictor hidden layer,
- * active counts, partial sums, output).  Barrier waits are bounded: a wait
- * that runs out sets a status bit (PI_ERR_DEVICE_CHECK from
- * pi_device_status on layers[0]) and the kernel returns. */
+ * For B <= 2 each group of up to PI_STACK_LAYERS_PER_LAUNCH layers is one
+ * cooperative launch with one CTA per SM and two grid-wide barriers per layer
+ * (predictor hidden layer; output).  The split sums of y are added as 2^-32
+ * fixed-point int64 values, so y is bitwise reproducible; a partial sum of
+ * magnitude 2^23 or more sets the layer's device status (PI_ERR_DEVICE_CHECK
+ * from pi_device_status on layers[0]).  Barrier waits are bounded: a wait that
+ * runs out sets the same status and the kernel returns. */
 pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers,
                            const uint16_t *x, int32_t B, int32_t *idx,
                            int32_t *count, float *y, void *ws,
                            size_t ws_bytes, void *stream);
+
+/* The same decode step with each layer's input formed from the previous
+ * layer's output on the device (a decoder's data dependence; the attention
+ * blocks between FFN blocks are outside this library):
+ *   x[l] = fp16(y[l-1] / RMS(y[l-1])) for l >= 1, per token,
+ *   RMS(v) = sqrt(mean(v^2) + 1e-12) in binary32.
+ *   x  device fp16 [n_layers, B, d]: x[0] is the input; x[1..n_layers) are
+ *      overwritten with the inputs the layers used.
+ * Other arguments, results and errors as pi_stack_forward.  No input of
+ * layer l >= 1 is read before layer l - 1's y is complete. */
+pi_status pi_stack_forward_chained(pi_layer *const *layers, int32_t n_layers,
+                                   uint16_t *x, int32_t B, int32_t *idx,
+                                   int32_t *count, float *y, void *ws,
+                                   size_t ws_bytes, void *stream);
 
 /* pi_sparse_ffn without a workspace, for callers that cannot allocate device
  * memory when they call in (for example a serving framework that has already
@@ -242,8 +258,9 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers,
  * pointers), batches of 1 or 2 tokens only.  The split partial sums live in a
  * fixed 16 MiB device array inside the library (reserved on every GPU that
  * loads it, until the process exits); a call whose d and B need more than
- * that (4 * splits * B * d bytes, splits = the SM count, or 4x it for d < 4096)
- * returns PI_ERR_UNSUPPORTED without launching.  Nothing is allocated and
+ * that (4 * splits * B * d bytes, splits = the CTAs of the fused kernel: the
+ * SM count times 4 for d <= 1024, 3 for d <= 1280, 2 for d <= 2048 and 1
+ * above) returns PI_ERR_UNSUPPORTED without launching.  Nothing is allocated and
  * nothing in the array has to start at zero.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call outside any
@@ -283,10 +300,12 @@ pi_status pi_layer_set_timing_events(pi_layer *layer, void *ev_before, void *ev_
  * neurons are the few that are activated most often; section 3.1 Finding 1).
  * n_hot = how many leading neurons of the order given to pi_layer_create are
  * hot (e.g. those a profile shows active on more than half of the tokens).
- * pi_layer_forward / pi_stack_forward (B <= 2) then start streaming those
- * neurons' rows towards L2 at the start of the layer, before the predictor
- * has decided, so that HBM is busy during the predictor phases.  Results do
- * not change; a hot neuron the predictor leaves out only costs bandwidth.
+ * pi_layer_forward / pi_stack_forward (B <= 2) then load the rows of each
+ * SM slice's leading hot places (at most a few per slice, as many as its
+ * registers hold) while the previous layer finishes and the predictor runs,
+ * before the predictor has decided, so that HBM is busy during the predictor
+ * phases.  Results do not change; a hot neuron the predictor leaves out only
+ * costs bandwidth.
  * 0 (the default) disables it.  0 <= n_hot <= ffn. */
 pi_status pi_layer_set_hot_count(pi_layer *layer, int32_t n_hot);
 

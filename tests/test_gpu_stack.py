@@ -173,3 +173,79 @@ def test_hot_hint_changes_no_result(pi):
     assert torch.equal(y0, y1) and torch.equal(cnt0, cnt1)
     with pytest.raises(pi.PiError):
         layers[0].set_hot_count(8193)
+
+
+def _chained_x_ref(y_prev) -> np.ndarray:
+    """The chained input of the next layer from y [B, d]: y / RMS(y) per token,
+    RMS(v) = sqrt(mean(v^2) + 1e-12), in float64 (the GPU rounds its binary32
+    result to fp16, so the two agree within one fp16 step)."""
+    y = np.asarray(y_prev, dtype=np.float64)
+    return y / np.sqrt((y * y).mean(axis=-1, keepdims=True) + 1e-12)
+
+
+def _check_fp16_within_one_step(x_gpu, ref):
+    ref16 = ref.astype(np.float16)
+    step = np.spacing(np.abs(ref16)).astype(np.float64)
+    diff = np.abs(np.asarray(x_gpu, np.float64) - ref16.astype(np.float64))
+    assert (diff <= step).all(), f"chained input off by {float((diff / step).max()):.2f} fp16 steps"
+
+
+@pytest.mark.parametrize("act,d,ffn,r,B,n", [("relu", 1024, 4096, 64, 1, 5),
+                                             ("reglu", 2048, 3000, 40, 2, 4),
+                                             ("relu", 4096, 6000, 256, 1, 35),
+                                             ("relu", 1024, 2048, 64, 3, 4)])
+def test_chained_stack(pi, act, d, ffn, r, B, n):
+    """Decode chain: layer l >= 1 takes fp16(y_{l-1} / RMS(y_{l-1})), formed on
+    the device (across launch boundaries too: 35 layers span two launches).
+    Every checked layer is compared with the oracle on the input the GPU used."""
+    spec = LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1)
+    ts, layers = _stack(pi, spec, n, seed=d + 7 * ffn + B)
+    for layer in layers:
+        layer.set_hot_count(ffn // 5)
+    x = torch.zeros(n, B, d, dtype=torch.float16, device="cuda")
+    x[0] = make_tokens(d, B, seed=41 + B).cuda()
+    x_first = x[0].clone()
+    y = torch.empty(n, B, d, dtype=torch.float32, device="cuda")
+    idx = torch.full((n, ffn), -1, dtype=torch.int32, device="cuda")
+    count = torch.empty(n, dtype=torch.int32, device="cuda")
+    pi.stack_forward(layers, x, y, idx=idx, count=count, chained=True)
+    x2 = torch.zeros_like(x)
+    x2[0] = x_first
+    y2 = torch.empty_like(y)
+    pi.stack_forward(layers, x2, y2, idx=idx.clone(), count=count.clone(), chained=True)
+    torch.cuda.synchronize()
+    assert torch.equal(x[0], x_first), "the chained step must not overwrite x[0]"
+    assert torch.equal(y, y2) and torch.equal(x, x2), "chained step not bitwise reproducible"
+    xc, yc = x.cpu(), y.cpu().numpy()
+    for l in range(1, n):
+        _check_fp16_within_one_step(xc[l].numpy(), _chained_x_ref(yc[l - 1]))
+    check = list(range(n)) if n <= 6 else [0, 1, 17, 31, 32, 34]
+    for l in check:
+        c = int(count[l].item())
+        S = idx[l, :c].cpu().numpy().astype(np.int64)
+        _check_layer(ts[l], xc[l], yc[l], S, perm=layers[l].perm())
+    assert layers[0].device_status() == 0
+
+
+@pytest.mark.parametrize("act,d,ffn,r,B", [("relu", 4096, 8192, 128, 1), ("relu", 4096, 8192, 128, 2),
+                                           ("reglu", 2048, 6000, 64, 1), ("relu", 8192, 4096, 64, 1)])
+def test_dense_layer_many_windows(pi, act, d, ffn, r, B):
+    """About 60% of the neurons active: every CTA's list spans several row
+    windows, including the windows' shared-memory extension slots."""
+    n = 2
+    spec = LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.6)
+    ts, layers = _stack(pi, spec, n, seed=d + ffn + 3 * B)
+    for layer in layers:
+        layer.set_hot_count(ffn // 3)
+    x = make_tokens(d, n * B, seed=77 + B).view(n, B, d)
+    y = torch.empty(n, B, d, dtype=torch.float32, device="cuda")
+    idx = torch.full((n, ffn), -1, dtype=torch.int32, device="cuda")
+    count = torch.empty(n, dtype=torch.int32, device="cuda")
+    pi.stack_forward(layers, x.cuda(), y, idx=idx, count=count)
+    torch.cuda.synchronize()
+    assert int(count.min().item()) > ffn // 3
+    for l in range(n):
+        c = int(count[l].item())
+        _check_layer(ts[l], x[l], y[l].cpu().numpy(), idx[l, :c].cpu().numpy().astype(np.int64),
+                     perm=layers[l].perm())
+    assert layers[0].device_status() == 0
