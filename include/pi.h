@@ -224,12 +224,12 @@ pi_status pi_layer_forward(pi_layer *layer, const uint16_t *x, int32_t B,
  *   y       device fp32 [n_layers, B, d]
  *   ws      workspace of pi_workspace_bytes(layers[0], B) bytes
  * For B <= 2 each group of up to PI_STACK_LAYERS_PER_LAUNCH layers is one
- * cooperative launch with one CTA per SM and two grid-wide barriers per layer
- * (predictor hidden layer; output).  The split sums of y are added as 2^-32
- * fixed-point int64 values, so y is bitwise reproducible; a partial sum of
- * magnitude 2^23 or more sets the layer's device status (PI_ERR_DEVICE_CHECK
- * from pi_device_status on layers[0]).  Barrier waits are bounded: a wait that
- * runs out sets the same status and the kernel returns. */
+ * cooperative launch with one CTA per SM and three grid-wide barriers per
+ * layer (predictor hidden layer; split partial sums; output).  The partial
+ * sums of y are added in a fixed order, so y is bitwise reproducible.  Barrier
+ * waits are bounded: a wait that runs out sets a status bit
+ * (PI_ERR_DEVICE_CHECK from pi_device_status on layers[0]) and the kernel
+ * returns. */
 pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers,
                            const uint16_t *x, int32_t B, int32_t *idx,
                            int32_t *count, float *y, void *ws,
