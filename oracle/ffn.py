@@ -114,7 +114,7 @@ def active_union(mask) -> np.ndarray:
     return np.flatnonzero(m.any(axis=0)).astype(np.int64)
 
 
-def logit_error_bound(L: OracleLayer, x, h=None) -> np.ndarray:
+def logit_error_bound(L: OracleLayer, x, h=None, split: bool = False) -> np.ndarray:
     """Bound on |l_fp32 - l| for a GPU that computes h and l in binary32.
 
     Products of two fp16 values are exact in binary32; a dot of n terms has
@@ -123,6 +123,14 @@ def logit_error_bound(L: OracleLayer, x, h=None) -> np.ndarray:
     tau_i = 2 * [gamma_{r+1} (sum_k |W_p2_ik| (h_k + e_k) + |c_i|)
                  + sum_k |W_p2_ik| e_k],
     the leading 2 being slack.  Decisions with |l_i| > tau_i are forced.
+
+    split: the form in which h enters fp16 products as a pair h32 = hi + lo + s
+    (hi = fp16(h32), lo = fp16(h32 - hi)), as on tensor cores.  Then
+    |s_k| <= 2^-22 |h32_k| + 2^-25 (two fp16 roundings; the 2^-25 covers lo in
+    fp16's subnormal range), the sum runs over 2r products plus c, and
+    |hi| + |lo| <= |h32| (1 + 2^-10), so
+    tau_i = 2 * [gamma_{2r+1} (sum_k |W_p2_ik| m_k + |c_i|) + sum_k |W_p2_ik| (e_k + s_k)]
+    with m_k = (h_k + e_k)(1 + 2^-10) and s_k = 2^-22 (h_k + e_k) + 2^-25.
     """
     x = _f64(x).reshape(-1, L.d)
     if h is None:
@@ -131,8 +139,30 @@ def logit_error_bound(L: OracleLayer, x, h=None) -> np.ndarray:
     A2 = np.abs(_f64(L.W_p2))
     e = _gamma(L.d) * (np.abs(x) @ A1.T)                 # [B, r]
     cabs = 0.0 if L.c_p is None else np.abs(_f64(L.c_p))[None, :]
-    tau = _gamma(L.rank + 1) * ((h + e) @ A2.T + cabs) + e @ A2.T
+    if not split:
+        tau = _gamma(L.rank + 1) * ((h + e) @ A2.T + cabs) + e @ A2.T
+    else:
+        s = fp16_pair_error_bound(h + e)
+        m = (h + e) * (1.0 + 2.0 ** -10)
+        tau = _gamma(2 * L.rank + 1) * (m @ A2.T + cabs) + (e + s) @ A2.T
     return 2.0 * tau
+
+
+def fp16_pair_error_bound(v) -> np.ndarray:
+    """Bound on |v - hi - lo| for the fp16 pair of binary32 values of magnitude
+    at most |v|: the two fp16 roundings leave at most 2^-22 |v| relative, and
+    at most 2^-25 absolute once lo falls in fp16's subnormal range (spacing
+    2^-24)."""
+    return 2.0 ** -22 * np.abs(_f64(v)) + 2.0 ** -25
+
+
+def fp16_pair(v) -> tuple:
+    """The fp16 pair (hi, lo) of binary32 values v: hi = fp16(v), lo = fp16(v - hi),
+    v - hi formed in binary32 (exact: hi is v rounded to a coarser grid)."""
+    v32 = np.asarray(v, dtype=np.float32)
+    hi = v32.astype(np.float16)
+    lo = (v32 - hi.astype(np.float32)).astype(np.float16)
+    return hi, lo
 
 
 # --------------------------------------------------------------------------

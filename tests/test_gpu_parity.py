@@ -53,7 +53,7 @@ def test_predict(pi, shape, B):
     m_gpu = mask.cpu().numpy().astype(bool)
     h = O.predictor_hidden(L, x)
     l = O.predictor_logits(L, h)
-    tau = O.logit_error_bound(L, x, h)
+    tau = O.logit_error_bound(L, x, h, split=B > 2)   # B > 2: tensor-core form
     assert (np.abs(l_gpu - l) <= tau).all()
     np.testing.assert_array_equal(m_gpu, l_gpu > 0)
     forced = np.abs(l) > tau

@@ -30,8 +30,13 @@ def _check_layer(t, x, y, S, perm=None):
     L = O.OracleLayer.from_tensors(t)
     if perm is not None:
         L = O.permute_layer(L, perm)
-    r = O.predicted_forward(L, x)
-    band = check_union_set(S, r["l"], r["tau"])
+    x2 = np.atleast_2d(np.asarray(x))
+    if x2.shape[0] > 2:       # batched path: h enters the logits as an fp16 pair
+        h = O.predictor_hidden(L, x2)
+        band = check_union_set(S, O.predictor_logits(L, h), O.logit_error_bound(L, x2, h, split=True))
+    else:
+        r = O.predicted_forward(L, x)
+        band = check_union_set(S, r["l"], r["tau"])
     check_y(y, oracle_y_for_valid_set(L, x, S))
     return band
 
@@ -132,8 +137,9 @@ def test_bench_configuration_sampled(pi):
 @pytest.mark.parametrize("name", ["llama2_70b_reglu", "falcon40b_stack", "opt175b_stack"])
 def test_full_size_layer(pi, name):
     """One layer at the full per-layer size of each larger workload, batch 1
-    through the persistent step, plus the workload's larger batches through
-    the batched path (union active set)."""
+    through the persistent step, plus the workload's larger batches and its
+    prompt pass (128 tokens at once for the OPT-175B shape: the low-sparsity
+    union, several hundred 128-row tiles) through the batched path."""
     cfg = config_by_name(name)
     spec = cfg.layer
     dev = torch.device("cuda")
@@ -142,17 +148,83 @@ def test_full_size_layer(pi, name):
     th = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
     del t
     L = O.permute_layer(O.OracleLayer.from_tensors(th), layer.perm())
-    for B in sorted(set((1,) + tuple(b for b in cfg.batches if b > 1))):
+    batches = (1,) + tuple(b for b in cfg.batches if b > 1) + ((cfg.prompt,) if cfg.prompt else ())
+    for B in sorted(set(batches)):
         x = make_tokens(spec.d, B, seed=sub_seed(cfg.seed, B, "full_size_x"))
         y, idx, count = layer.forward(x.to(dev))
         torch.cuda.synchronize()
         S = idx[:int(count.item())].cpu().numpy().astype(np.int64)
         h = O.predictor_hidden(L, x)
-        check_union_set(S, O.predictor_logits(L, h), O.logit_error_bound(L, x, h))
-        rows = [0, B - 1] if B > 2 else list(range(B))
+        check_union_set(S, O.predictor_logits(L, h), O.logit_error_bound(L, x, h, split=B > 2))
+        rows = [0, B // 2, B - 1] if B > 2 else list(range(B))
         y_ref = O.sparse_ffn(L, x[rows], S)
         check_y(y.cpu().numpy()[rows], y_ref)
+        if B == cfg.prompt:
+            assert S.size > 0.9 * spec.ffn      # the prompt's union is nearly dense
     assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["opt_layer_d1024", "opt7b_stack", "llama2_70b_reglu",
+                                  "llama2_70b_swiglu", "falcon40b_stack", "opt175b_stack"])
+def test_full_size_layer_literal_predictor(pi, name):
+    """The predictor exactly as the pages state it (no output bias: c_p = 0,
+    so about half of the neurons are predicted active), one full-size layer
+    of each workload, batch 1 (persistent step) and batch 8 (batched path)."""
+    cfg = config_by_name(name)
+    spec = cfg.layer
+    dev = torch.device("cuda")
+    t = make_layer(spec, cfg.seed, 0, device=dev)
+    t["c_p"] = None
+    layer = pi.Layer.from_dict(t)
+    th = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    del t
+    L = O.permute_layer(O.OracleLayer.from_tensors(th), layer.perm())
+    assert L.c_p is None
+    for B in (1, 8):
+        x = make_tokens(spec.d, B, seed=sub_seed(cfg.seed, B, "literal_x"))
+        y, idx, count = layer.forward(x.to(dev))
+        torch.cuda.synchronize()
+        S = idx[:int(count.item())].cpu().numpy().astype(np.int64)
+        h = O.predictor_hidden(L, x)
+        check_union_set(S, O.predictor_logits(L, h), O.logit_error_bound(L, x, h, split=B > 2))
+        if B == 1:
+            assert 0.35 * spec.ffn < S.size < 0.65 * spec.ffn     # symmetric logits: about half
+        rows = [0, B - 1]
+        check_y(y.cpu().numpy()[rows], O.sparse_ffn(L, x[rows], S))
+    assert layer.device_status() == 0
+
+
+def test_bench_configuration_all_layers_several_tokens(pi):
+    """The OPT-7B-shaped stack as the benchmark builds it (32 layers,
+    hot-first order from a 10k-token profile, one persistent launch per
+    token): four tokens, every layer's active list and output against the
+    oracle."""
+    import bench
+    cfg = config_by_name("opt7b_stack")
+    spec = cfg.layer
+    dev = torch.device("cuda")
+    layers, _ = bench.build_stack(cfg, dev, cfg.layers, keep_host_layers=0)
+    T, Lc = 4, cfg.layers
+    X = make_tokens(spec.d, T * Lc, sub_seed(cfg.seed, 1000, "bench_x"), dev).view(T, Lc, 1, spec.d)
+    ws = layers[0].workspace(1)
+    ys = torch.empty(T, Lc, 1, spec.d, dtype=torch.float32, device=dev)
+    idx = torch.full((T, Lc, spec.ffn), -1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(T, Lc, dtype=torch.int32, device=dev)
+    for tok in range(T):
+        pi.stack_forward(layers, X[tok].contiguous(), ys[tok], idx=idx[tok], count=cnt[tok], ws=ws)
+    torch.cuda.synchronize()
+    assert layers[0].device_status() == 0
+    Xh, Yh, Ih, Ch = X.cpu(), ys.cpu().numpy(), idx.cpu().numpy(), cnt.cpu().numpy()
+    for l in range(Lc):
+        t = make_layer(spec, cfg.seed, l, device=dev)
+        th = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+        del t
+        L = O.permute_layer(O.OracleLayer.from_tensors(th), layers[l].perm())
+        for tok in range(T):
+            S = Ih[tok, l, :Ch[tok, l]].astype(np.int64)
+            r = O.predicted_forward(L, Xh[tok, l])
+            check_union_set(S, r["l"], r["tau"])
+            check_y(Yh[tok, l], oracle_y_for_valid_set(L, Xh[tok, l], S))
 
 
 def test_hot_hint_changes_no_result(pi):

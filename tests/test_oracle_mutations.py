@@ -44,6 +44,8 @@ MUTATIONS = [
     ("logit-band-drops-h-error", "oracle/ffn.py",
      "tau = _gamma(L.rank + 1) * ((h + e) @ A2.T + cabs) + e @ A2.T",
      "tau = _gamma(L.rank + 1) * (h @ A2.T + cabs)"),
+    ("fp16-pair-drops-subnormal-term", "oracle/ffn.py",
+     "return 2.0 ** -22 * np.abs(_f64(v)) + 2.0 ** -25", "return 2.0 ** -22 * np.abs(_f64(v))"),
     ("preact-band-drops-bias", "oracle/ffn.py",
      "s = np.abs(x) @ np.abs(_f64(Wg)).T + np.abs(_f64(L.b))[None, :]",
      "s = np.abs(x) @ np.abs(_f64(Wg)).T"),

@@ -432,3 +432,52 @@ def test_swiglu_sparse_sums_split_the_dense_sum_and_match_brute_force():
     bf = brute.forward({k: (v.numpy() if hasattr(v, "numpy") else v) for k, v in t.items()}, x.numpy())
     assert bf["S"] == list(S)
     assert np.allclose(np.array(bf["y"]), r["y"], rtol=1e-12, atol=1e-14)
+
+
+def test_fp16_pair_error_bound():
+    """The hi/lo fp16 split of binary32 values (the tensor-core form of h)
+    stays within fp16_pair_error_bound, on random values over many binades
+    and on hand-made values where each term of the bound is the one that
+    matters."""
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal(200000) * np.exp2(rng.integers(-12, 12, 200000))).astype(np.float32)
+    # 2^-6 + 3 * 2^-27: hi = 2^-6, the remainder 0.375 * 2^-24 rounds to lo = 0
+    # (fp16 subnormal spacing 2^-24): an error of 3 * 2^-27, above the relative
+    # term 2^-22 * 2^-6 = 2^-28; only the 2^-25 term covers it
+    sub = np.float32(2.0 ** -6 + 3 * 2.0 ** -27)
+    # 1 + 2^-11 + 2^-22 + 2^-23: the remainder needs more bits than fp16 keeps
+    rel = np.float32(1 + 2.0 ** -11 + 2.0 ** -22 + 2.0 ** -23)
+    v = np.concatenate([v, [sub, -sub, rel, -rel]]).astype(np.float32)
+    hi, lo = O.fp16_pair(v)
+    err = np.abs(v.astype(np.float64) - hi.astype(np.float64) - lo.astype(np.float64))
+    bound = O.fp16_pair_error_bound(v)
+    assert (err <= bound).all()
+    assert err[-4] == 3 * 2.0 ** -27 and err[-4] > 2.0 ** -22 * float(sub)
+    assert err[-2] > 0
+
+
+def test_logit_error_bound_split_covers_the_tensor_core_form():
+    """Logits formed as on tensor cores (h in binary32, split into an fp16
+    pair, 2r fp16 products summed in binary32 in two orders) stay within the
+    split form of the bound, which is never below the plain one."""
+    spec = LayerSpec(d=512, ffn=1024, rank=64, mean_f=0.1)
+    L = O.OracleLayer.from_tensors(make_layer(spec, 23))
+    X = make_tokens(512, 3, seed=24)
+    W2 = L.W_p2.astype(np.float32)
+    for t in range(3):
+        x16 = X[t].numpy()
+        h32 = np.maximum(0, _fp32_sequential(L.W_p1, x16.astype(np.float32))).astype(np.float32)
+        hi, lo = O.fp16_pair(h32)
+        h = O.predictor_hidden(L, X[t:t + 1])
+        l = O.predictor_logits(L, h)[0]
+        tau_s = O.logit_error_bound(L, X[t:t + 1], h, split=True)[0]
+        assert (tau_s >= O.logit_error_bound(L, X[t:t + 1], h)[0]).all()
+        for order in (0, 1):
+            acc = np.zeros(L.ffn, np.float32)
+            pairs = [(W2[:, k] * hi[k].astype(np.float32), W2[:, k] * lo[k].astype(np.float32))
+                     for k in range(L.rank)]
+            seq = [p for pr in pairs for p in pr] if order == 0 else [pr[1] for pr in pairs] + [pr[0] for pr in pairs]
+            for term in seq:
+                acc = (acc + term.astype(np.float32)).astype(np.float32)
+            acc = (acc + L.c_p.astype(np.float32)).astype(np.float32)
+            assert (np.abs(acc.astype(np.float64) - l) <= tau_s).all()
