@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     lib_path,
     profile_activations,
     stack_forward,
+    stack_forward_host,
 )
 
 __all__ = [
@@ -33,4 +34,5 @@ __all__ = [
     "lib_path",
     "profile_activations",
     "stack_forward",
+    "stack_forward_host",
 ]

@@ -61,6 +61,8 @@ _SIG = {
     "pi_layer_forward": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
     "pi_stack_forward": (C.c_int, [_p, _i32, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
     "pi_stack_forward_chained": (C.c_int, [_p, _i32, _p, _i32, _p, _p, _p, _p, C.c_size_t, _p]),
+    "pi_stack_forward_host": (C.c_int, [_p, _i32, _i32, _p, _i32, _p, _p, _p, _p, _p, _i32, _p,
+                                        C.c_size_t, _p]),
     "pi_profile_activations": (C.c_int, [C.POINTER(pi_layer_desc), _p, _i32, _p, _p]),
     "pi_hot_first_perm": (C.c_int, [_p, _i32, _p]),
     "pi_device_status": (C.c_int, [_p, _p]),
@@ -296,6 +298,33 @@ def stack_forward(layers, x, y, idx=None, count=None, ws=None, stream=None, hand
     _check(fn(handles, n, _ptr(x), B, _ptr(idx), _ptr(count), _ptr(y), _ptr(ws), ws.numel(),
               _stream(stream)), name)
     return y
+
+
+def stack_forward_host(layers, x_host, y_host, x_dev, y_dev, idx=None, count=None, ws=None,
+                       stream=None, handles=None, chained=False):
+    """T decode steps from host buffers in one library call: x_host [T, L, B, d]
+    fp16 (pinned) is copied into x_dev, each token runs through the stack, and
+    y_dev is copied into y_host [T, L, B, d] fp32 (pi_stack_forward_host)."""
+    if x_host.is_cuda or y_host.is_cuda:
+        raise TypeError("x_host and y_host must be host tensors")
+    _req(x_dev, torch.float16, "x_dev")
+    _req(y_dev, torch.float32, "y_dev")
+    if not (x_host.is_contiguous() and y_host.is_contiguous()):
+        raise ValueError("x_host and y_host must be contiguous")
+    if x_host.dtype != torch.float16 or y_host.dtype != torch.float32:
+        raise TypeError("x_host must be float16 and y_host float32")
+    T, n, B = int(x_host.shape[0]), len(layers), int(x_host.shape[2])
+    if x_host.shape != x_dev.shape or y_host.shape != y_dev.shape or tuple(x_host.shape[:2]) != (T, n):
+        raise ValueError("x_host/x_dev/y_host/y_dev must all be [T, n_layers, B, d]")
+    if handles is None:
+        handles = (C.c_void_p * n)(*[l.handle.value for l in layers])
+    if ws is None:
+        ws = layers[0].workspace(B)
+    _check(lib.pi_stack_forward_host(handles, n, T, C.c_void_p(x_host.data_ptr()), B,
+                                     C.c_void_p(y_host.data_ptr()), _ptr(x_dev), _ptr(y_dev), _ptr(idx),
+                                     _ptr(count), 1 if chained else 0, _ptr(ws), ws.numel(), _stream(stream)),
+           "pi_stack_forward_host")
+    return y_host
 
 
 def profile_activations(t: dict, x: torch.Tensor, counts: Optional[torch.Tensor] = None,

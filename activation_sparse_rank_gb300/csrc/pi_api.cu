@@ -182,6 +182,8 @@ pi_status check_desc(const pi_layer_desc *D) {
 
 namespace pi {
 
+void clear_error() { g_err[0] = 0; }
+
 pi_status fail(pi_status s, const char *fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -672,6 +674,31 @@ pi_status pi_stack_forward_chained(pi_layer *const *layers, int32_t n_layers, ui
   g_err[0] = 0;
   return stack_forward_impl(layers, n_layers, x, x, B, idx, count, y, ws, ws_bytes, stream, true,
                             "pi_stack_forward_chained with more than 2 tokens");
+}
+
+pi_status pi_stack_forward_host(pi_layer *const *layers, int32_t n_layers, int32_t T,
+                                const uint16_t *x_host, int32_t B, float *y_host, uint16_t *x_dev,
+                                float *y_dev, int32_t *idx, int32_t *count, int32_t chained,
+                                void *ws, size_t ws_bytes, void *stream) {
+  g_err[0] = 0;
+  if (T < 1) return pi::fail(PI_ERR_INVALID_ARG, "T=%d: need at least one token", T);
+  if (!x_host || !y_host) return pi::fail(PI_ERR_INVALID_ARG, "x_host and y_host must be non-NULL");
+  if (!layers || n_layers < 1 || !layers[0]) return pi::fail(PI_ERR_INVALID_ARG, "layers is NULL or n_layers < 1");
+  if (B < 1 || B > PI_MAX_BATCH) return pi::fail(PI_ERR_INVALID_ARG, "B=%d: need 1 <= B <= %d", B, PI_MAX_BATCH);
+  if (!x_dev || !aligned16(x_dev) || !y_dev || !aligned16(y_dev))
+    return pi::fail(PI_ERR_INVALID_ARG, "x_dev and y_dev must be non-NULL and 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t per_tok = (size_t)n_layers * B * layers[0]->d;     // elements of one token's x or y
+  PI_TRY_CUDA(cudaMemcpyAsync(x_dev, x_host, sizeof(uint16_t) * per_tok * T, cudaMemcpyHostToDevice, s));
+  for (int t = 0; t < T; ++t) {
+    uint16_t *xt = x_dev + per_tok * t;
+    const pi_status st = stack_forward_impl(layers, n_layers, xt, xt, B, idx, count ? count + (size_t)t * n_layers : nullptr,
+                                            y_dev + per_tok * t, ws, ws_bytes, stream, chained != 0,
+                                            "pi_stack_forward_host with more than 2 tokens");
+    if (st != PI_OK) return st;
+  }
+  PI_TRY_CUDA(cudaMemcpyAsync(y_host, y_dev, sizeof(float) * per_tok * T, cudaMemcpyDeviceToHost, s));
+  return PI_OK;
 }
 
 pi_status pi_profile_activations(const pi_layer_desc *D, const uint16_t *x, int32_t T,

@@ -42,6 +42,7 @@ namespace pi {
 
 // ---- errors ---------------------------------------------------------------
 pi_status fail(pi_status s, const char *fmt, ...);
+void clear_error();                 // empty this thread's pi_last_error text
 pi_status cuda_fail(cudaError_t e, const char *what);
 
 #define PI_TRY_CUDA(call)                                     \

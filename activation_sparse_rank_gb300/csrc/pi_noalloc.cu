@@ -8,10 +8,14 @@
 // scratch (the per-CTA partial sums of the split reduction) in a file-scope
 // device array, so the call needs nothing beyond its inputs and outputs.
 //
-// The array is reserved in every GPU that loads the library, for as long as
-// the process lives, so it is kept modest: kScratchBytes below.  All calls
-// share it: calls whose kernels overlap on the GPU (different streams, or
-// different host threads) race on it and must be serialised by the caller.
+// The array is reserved on a GPU when that GPU loads this file's module (with
+// CUDA's default lazy module loading: at this entry point's first call on the
+// GPU) and stays until the process exits, so it is kept modest: kScratchBytes
+// below.  All calls share it: calls whose kernels overlap on the GPU
+// (different streams, or different host threads) race on it and must be
+// serialised by the caller.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "pi_internal.cuh"
@@ -27,20 +31,48 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct Cached {
+  CUcontext ctx = nullptr;   // the context the address belongs to
+  void *ptr = nullptr;
+};
+Cached g_cache[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once
-// per device (host code must not use the symbol itself as a device pointer).
+// The driver's cuCtxGetCurrent, looked up through the runtime (the library
+// does not link libcuda).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+// Device address of the scratch array in the current context of device dev.
+// Host code must not use the symbol itself as a device pointer.  The address
+// is looked up once per context: a new context (after cudaDeviceReset, or
+// after the primary context was released and created again) looks it up anew.
 pi_status scratch_for_device(int dev, void **out) {
   if (dev < 0 || dev >= kMaxDevices) return pi::fail(PI_ERR_UNSUPPORTED, "device %d out of range", dev);
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return pi::fail(PI_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return pi::fail(PI_ERR_CUDA, "cuCtxGetCurrent failed");
+  Cached &c = g_cache[dev];
+  if (!c.ptr || !ctx || ctx != c.ctx) {
     void *p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // makes the context current
     if (e != cudaSuccess) return pi::cuda_fail(e, "cudaGetSymbolAddress(g_noalloc_scratch)");
-    g_scratch_ptr[dev] = p;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return pi::fail(PI_ERR_CUDA, "no current context on device %d", dev);
+    c.ctx = ctx;
+    c.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = c.ptr;
   return PI_OK;
 }
 
@@ -49,6 +81,7 @@ pi_status scratch_for_device(int dev, void **out) {
 extern "C" pi_status pi_sparse_ffn_noalloc(pi_layer *L, const uint16_t *x, int32_t B,
                                            const int32_t *idx, const int32_t *count, float *y,
                                            void *stream) {
+  pi::clear_error();
   if (!L) return pi::fail(PI_ERR_INVALID_ARG, "layer is NULL");
   if (L->row_format != PI_ROWS_FP16)
     return pi::fail(PI_ERR_UNSUPPORTED, "pi_sparse_ffn_noalloc needs a layer with fp16 rows");

@@ -14,7 +14,7 @@ from typing import List, Optional
 
 import torch
 
-from .binding import PI_STACK_LAYERS_PER_LAUNCH, Layer, stack_forward
+from .binding import PI_STACK_LAYERS_PER_LAUNCH, Layer, stack_forward, stack_forward_host
 
 
 class SparseFFNStack:
@@ -93,12 +93,11 @@ class SparseFFNStack:
         self.graph.replay()
 
     def run_host(self, x_host: torch.Tensor, y_host: torch.Tensor, stream=None):
-        """One step from host memory: copy x_host [T, L, B, d] (pinned fp16) in,
-        replay the step, copy y [T, L, B, d] fp32 out to pinned y_host."""
-        if self.graph is None:
-            self.build_graph()
+        """One step from host memory through one library call
+        (pi_stack_forward_host): x_host [T, L, B, d] (pinned fp16) is copied
+        in, every token runs through the stack, y [T, L, B, d] fp32 is copied
+        out to pinned y_host; all on `stream`, not captured in a graph."""
         s = stream or torch.cuda.current_stream()
-        with torch.cuda.stream(s):
-            self.x.copy_(x_host, non_blocking=True)
-            self.graph.replay()
-            y_host.copy_(self.y, non_blocking=True)
+        stack_forward_host(self.layers, x_host, y_host, self.x, self.y, idx=self.idx,
+                           count=self.count, ws=self.ws, stream=s, handles=self.handles,
+                           chained=self.chained)

@@ -60,6 +60,10 @@ def parse():
     ap.add_argument("--chained", action="store_true",
                     help="time the chained decode step as the main line (x of layer l+1 = "
                          "fp16(y_l / RMS(y_l)) formed on the device)")
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="copies of the layer stack, each at its own addresses, run one after "
+                         "another (0: enough copies that the weights are at least 4x the L2 "
+                         "cache, so that every step reads them from HBM)")
     ap.add_argument("--no-chained-line", action="store_true",
                     help="skip the chained-decode figure reported beside the main line")
     return ap.parse_args()
@@ -141,10 +145,15 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
-def build_stack(cfg, device, n_layers, keep_host_layers, rows="fp16", hot_frac=HOT_FRAC):
+def build_stack(cfg, device, n_layers, keep_host_layers, rows="fp16", hot_frac=HOT_FRAC,
+                replicas: int = 1):
+    """The workload's layers (and, with replicas > 1, that many copies of the
+    whole stack one after another, each copy's weights at their own device
+    addresses)."""
     import activation_sparse_rank_gb300 as pi
     spec = cfg.layer
     layers, host_layers = [], []
+    copies = []
     for l in range(n_layers):
         t = make_layer(spec, cfg.seed, l, device=device)
         perm = None
@@ -159,12 +168,57 @@ def build_stack(cfg, device, n_layers, keep_host_layers, rows="fp16", hot_frac=H
         layer = pi.Layer.from_dict(t, perm=perm, rows=rows)
         layer.set_hot_count(n_hot)
         layers.append(layer)
+        for _ in range(replicas - 1):
+            c = pi.Layer.from_dict(t, perm=perm, rows=rows)
+            c.set_hot_count(n_hot)
+            copies.append(c)
         if l < keep_host_layers:
             host_layers.append({k: (v.cpu() if isinstance(v, torch.Tensor) else v)
                                 for k, v in t.items()})
         del t
     torch.cuda.synchronize()
+    if replicas > 1:          # copy r of layer l at position r * n_layers + l
+        per = replicas - 1
+        layers = layers + [copies[l * per + r] for r in range(per) for l in range(n_layers)]
     return layers, host_layers
+
+
+def hot_concentration(counts, share: float = 0.8) -> float:
+    """Smallest fraction of the neurons whose activation counts add up to
+    `share` of all activations (the hot neurons of the pages' power-law
+    locality: "a few neurons carry most activations")."""
+    c = np.sort(np.asarray(counts, dtype=np.float64))[::-1]
+    tot = c.sum()
+    if tot <= 0:
+        return 0.0
+    k = int(np.searchsorted(np.cumsum(c), share * tot - 1e-9)) + 1
+    return k / c.size
+
+
+def profile_concentration(cfg, device, tokens: int = 4096) -> dict:
+    """The achieved hot concentration of layer 0 of a workload, from an
+    activation profile on the GPU (the configured profile length, else
+    `tokens` tokens)."""
+    import activation_sparse_rank_gb300 as pi
+    spec = cfg.layer
+    T = cfg.profile_tokens or tokens
+    t = make_layer(spec, cfg.seed, 0, device=device)
+    Xp = make_tokens(spec.d, T, sub_seed(cfg.seed, 0, "profile"), device)
+    counts = pi.profile_activations(t, Xp).cpu().numpy()
+    del t, Xp
+    return {"share_of_neurons_carrying_80pct": hot_concentration(counts, 0.8),
+            "mean_firing_rate": float(counts.mean() / T), "profile_tokens": T, "layer": 0}
+
+
+def auto_replicas(cfg, n_layers: int, device=None) -> int:
+    """Copies of an n_layers stack whose weights together reach 4x the L2."""
+    spec = cfg.layer
+    rows = 3 if spec.act in ("reglu", "swiglu") else 2
+    per_layer = 2 * spec.d * spec.ffn * rows + predictor_bytes(spec.d, spec.ffn, spec.rank)
+    l2 = (torch.cuda.get_device_properties(device).L2_cache_size if device is not None
+          else 129 * 1024 * 1024)
+    total = per_layer * n_layers
+    return max(1, -(-4 * l2 // total)) if total < 4 * l2 else 1
 
 
 def touched_bytes(cfg, counts: torch.Tensor, rows: str = "fp16") -> int:
@@ -245,7 +299,8 @@ def run_reference(args, cfg):
         "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(cfg, L_total, args.tokens or cfg.tokens, Bt,
-                                  int(os.environ.get("WORLD_SIZE", "1")), args.rows),
+                                  int(os.environ.get("WORLD_SIZE", "1")), args.rows, args.chained,
+                                  args.replicas or auto_replicas(cfg, L_total)),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{tot_p} (token, layer) pairs of layers 0..{n_layers - 1}, "
                                    f"{tot_t:.1f} s, batch {Bt}, scaled to a {L_total}-layer stack; numpy "
@@ -256,14 +311,18 @@ def run_reference(args, cfg):
 
 
 def workload_config(cfg, n_layers: int, T: int, Bt: int, world: int, rows: str = "fp16",
-                    chained: bool = False) -> dict:
+                    chained: bool = False, replicas: int = 1) -> dict:
     """The config object both arms print for one workload."""
     spec = cfg.layer
     weights = "fp16" if rows == "fp16" else "fp16 predictor; up/gate/down rows FP8 E4M3 with a per-row fp32 scale"
     return {"workload": cfg.description, "name": cfg.name, "d": spec.d, "ffn": spec.ffn,
-            "rank": spec.rank, "layers": n_layers, "tokens_per_step": T * Bt, "batch": Bt,
+            "rank": spec.rank, "layers": n_layers, "tokens_per_step": T * Bt * replicas, "batch": Bt,
+            "replicas": replicas,
             "act": spec.act, "weights": weights, "hot_first": bool(cfg.profile_tokens),
-            "l2": "inputs larger than L2: the distinct weight rows of a step exceed the 129 MB L2",
+            "l2": ("inputs larger than L2: the distinct weight rows of a step exceed the 129 MB L2"
+                   if replicas == 1 else
+                   f"inputs larger than L2: {replicas} copies of the stack at their own addresses, "
+                   "run one after another, hold at least 4x the 129 MB L2"),
             "parallelism": f"replicas{world}",
             "inputs": ("chained: x of layer l+1 = fp16(y_l / RMS(y_l)) on the device" if chained
                        else "independent seeded x ~ N(0, I) per (token, layer); layer l+1 starts "
@@ -319,11 +378,13 @@ def main():
     # the CPU baseline times the fp16 oracle; it belongs to the fp16 workload
     want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1 and Bt == 1 and rows == "fp16"
     t_setup = time.perf_counter()
+    R = args.replicas or auto_replicas(cfg, n_layers, device)
     layers, host_layers = build_stack(cfg, device, n_layers, keep_host_layers=2 if want_cpu else 0,
-                                      rows=rows)
+                                      rows=rows, replicas=R)
+    NL = len(layers)                      # layers one token passes: R copies of the stack
     stack = SparseFFNStack(layers, tokens=T, B=Bt, chained=args.chained)
-    X = make_tokens(spec.d, T * n_layers * Bt, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
-    stack.x.copy_(X.view(T, n_layers, Bt, spec.d))
+    X = make_tokens(spec.d, T * NL * Bt, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
+    stack.x.copy_(X.view(T, NL, Bt, spec.d))
     del X
     stack.build_graph()
     torch.cuda.synchronize()
@@ -340,25 +401,29 @@ def main():
     s.synchronize()
 
     clocks = ClockSampler(local)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    evs_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
     torch.cuda.synchronize()
-    ev0.record(s)
+    evs_step[0].record(s)
     with torch.cuda.stream(s):
-        for _ in range(args.steps):
+        for k in range(args.steps):
             stack.graph.replay()
-    ev1.record(s)
+            evs_step[k + 1].record(s)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, device=device)
+    step_ms = [evs_step[k].elapsed_time(evs_step[k + 1]) for k in range(args.steps)]
+    ms = max_over_ranks(evs_step[0].elapsed_time(evs_step[-1]) / args.steps, device=device)
     for layer in layers:
         if layer.device_status() != 0:
             raise RuntimeError("device check failed during the timed steps")
 
-    tokens_step = T * Bt
+    tokens_step = T * Bt * R            # tokens of the n_layers-layer workload per step
     value = tokens_step * world / (ms / 1000.0)
+    repeats = {"n": len(step_ms), "median_ms": statistics.median(step_ms), "min_ms": min(step_ms),
+               "max_ms": max(step_ms),
+               "median_tokens_per_s": tokens_step * world / (statistics.median(step_ms) / 1000.0),
+               "max_tokens_per_s": tokens_step * world / (min(step_ms) / 1000.0)}
     tb = touched_bytes(cfg, stack.count, rows)
     mean_S = float(stack.count.double().mean().item())
     eff_gbs = tb / (ms / 1000.0) / 1e9
@@ -372,7 +437,7 @@ def main():
         Td = min(16, T)
         dense_g = torch.cuda.CUDAGraph()
         ws = stack.ws
-        yd = torch.empty(n_layers, Bt, spec.d, dtype=torch.float32, device=device)
+        yd = torch.empty(NL, Bt, spec.d, dtype=torch.float32, device=device)
         with torch.cuda.stream(s):
             for li, layer in enumerate(layers):
                 layer.dense_ref(stack.x[0, li], yd[li], ws=ws, stream=s)
@@ -392,7 +457,7 @@ def main():
                 dense_g.replay()
         e1.record(s)
         torch.cuda.synchronize()
-        dense_tok_s = 3 * Td * Bt / (e0.elapsed_time(e1) / 1000.0)
+        dense_tok_s = 3 * Td * Bt * R / (e0.elapsed_time(e1) / 1000.0)
 
     # dominant kernel (the persistent step kernel, one launch per token)
     # timed inside a captured step with external event-record nodes
@@ -426,7 +491,7 @@ def main():
     cnt = stack.count[:Tr].cpu().numpy()
     # layers[0]'s timing hook brackets the launch that holds layer 0: the first
     # PI_STACK_LAYERS_PER_LAUNCH layers of a longer stack
-    L1 = min(n_layers, pi.PI_STACK_LAYERS_PER_LAUNCH)
+    L1 = min(NL, pi.PI_STACK_LAYERS_PER_LAUNCH)
     if Bt <= 2:   # the persistent step: predictor + rows of the launch's layers
         alg_bytes = (Tr * L1 * predictor_bytes(spec.d, spec.ffn, spec.rank)
                      + float(cnt[:, :L1].sum()) * bytes_per_active_neuron(spec.d, spec.act, rows))
@@ -506,6 +571,29 @@ def main():
                                 "layer l completes; only layer 0's x is an input"}
         del cst
 
+    # with copies, the same step over one copy (its weights may stay in L2)
+    warm = None
+    if R > 1:
+        st1 = SparseFFNStack(layers[:n_layers], tokens=T, B=Bt)
+        st1.x.copy_(stack.x[:, :n_layers])
+        st1.build_graph()
+        for _ in range(3):
+            with torch.cuda.stream(st1.stream):
+                st1.graph.replay()
+        st1.stream.synchronize()
+        w0 = torch.cuda.Event(enable_timing=True)
+        w1 = torch.cuda.Event(enable_timing=True)
+        w0.record(st1.stream)
+        with torch.cuda.stream(st1.stream):
+            for _ in range(5):
+                st1.graph.replay()
+        w1.record(st1.stream)
+        st1.stream.synchronize()
+        warm = {"value": 5 * T * Bt / (w0.elapsed_time(w1) / 1000.0), "unit": "tokens/s",
+                "what": "one copy of the stack, replayed: its weights can stay in L2"}
+        del st1
+    concentration = profile_concentration(cfg, device)
+
     cpu = None
     if want_cpu:
         xh_l = stack.x[:, :2].cpu()
@@ -519,7 +607,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": workload_config(cfg, n_layers, T, Bt, world, rows, args.chained),
+            "config": workload_config(cfg, n_layers, T, Bt, world, rows, args.chained, R),
             "effective_hbm_gbs": eff_gbs,
             "effective_frac_of_measured": eff_gbs / peak,
             "effective_frac_of_nominal_8tbs": eff_gbs / (NOMINAL_HBM_GBS),
@@ -528,6 +616,7 @@ def main():
             "speedup_vs_dense": value / world / dense_tok_s if dense_tok_s else None,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "chained_decode": chained_line,
+            "repeats": repeats, "warm_l2": warm, "hot_concentration": concentration,
             "gpu_launches": gpu_launches, "clocks": clk, "setup_s": setup_s,
         }
         print(json.dumps(line), flush=True)

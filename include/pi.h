@@ -249,6 +249,25 @@ pi_status pi_stack_forward_chained(pi_layer *const *layers, int32_t n_layers,
                                    int32_t *count, float *y, void *ws,
                                    size_t ws_bytes, void *stream);
 
+/* T decode steps from host memory in one call: copies x_host into x_dev,
+ * runs pi_stack_forward (or, with chained != 0, pi_stack_forward_chained) for
+ * each token t on x_dev[t] -> y_dev[t], and copies y_dev into y_host, all
+ * asynchronously on `stream` (the copies are part of the call, so a caller
+ * that times it from host buffers to host buffers times the copies too).
+ *   x_host  host fp16 [T, n_layers, B, d]; y_host host fp32 [T, n_layers, B, d]
+ *           (page-locked memory lets the copies run asynchronously at full
+ *           rate; pageable memory works, the copies then block the host)
+ *   x_dev   device fp16 [T, n_layers, B, d], y_dev device fp32 [T, n_layers, B, d]
+ *           (caller-owned staging; in chained mode x_dev[t][1..] is overwritten)
+ *   idx     device int32 [n_layers, ffn] (the last token's lists) or NULL (B <= 2)
+ *   count   device int32 [T, n_layers] or NULL (B <= 2)
+ * Errors as pi_stack_forward; nothing is launched after the first failure. */
+pi_status pi_stack_forward_host(pi_layer *const *layers, int32_t n_layers, int32_t T,
+                                const uint16_t *x_host, int32_t B, float *y_host,
+                                uint16_t *x_dev, float *y_dev, int32_t *idx,
+                                int32_t *count, int32_t chained, void *ws,
+                                size_t ws_bytes, void *stream);
+
 /* pi_sparse_ffn without a workspace, for callers that cannot allocate device
  * memory when they call in (for example a serving framework that has already
  * handed all GPU memory to its own pool, or a plug-in that receives only input
@@ -256,17 +275,20 @@ pi_status pi_stack_forward_chained(pi_layer *const *layers, int32_t n_layers,
  * convention of this library, not part of the method.
  * Same arguments and results as pi_sparse_ffn (x, idx, count, y device
  * pointers), batches of 1 or 2 tokens only.  The split partial sums live in a
- * fixed 16 MiB device array inside the library (reserved on every GPU that
- * loads it, until the process exits); a call whose d and B need more than
- * that (4 * splits * B * d bytes, splits = the CTAs of the fused kernel: the
- * SM count times 4 for d <= 1024, 3 for d <= 1280, 2 for d <= 2048 and 1
- * above) returns PI_ERR_UNSUPPORTED without launching.  Nothing is allocated and
- * nothing in the array has to start at zero.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) and caches it; make that first call outside any
- * stream capture.  All calls share the one array: calls whose kernels can
- * overlap on the GPU (other streams, other host threads) race on it and must
- * be serialised by the caller. */
+ * fixed 16 MiB device array inside the library, reserved on a GPU when that
+ * GPU loads the array (with CUDA's default lazy module loading: this entry
+ * point's first call on it; with CUDA_MODULE_LOADING=EAGER: when the library
+ * is loaded) and kept until the process exits.  A call whose d and B need
+ * more than that (4 * splits * B * d bytes, splits = the CTAs of the fused
+ * kernel: the SM count times 4 for d <= 1024, 3 for d <= 1280, 2 for
+ * d <= 2048 and 1 above) returns PI_ERR_UNSUPPORTED without launching.
+ * Nothing is allocated and nothing in the array has to start at zero.
+ * The array's device address is looked up (cudaGetSymbolAddress) on the first
+ * call in each device context and cached for that context; a new context (for
+ * example after cudaDeviceReset) looks it up again.  Make the first call in a
+ * context outside any stream capture.  All calls share the one array: calls
+ * whose kernels can overlap on the GPU (other streams, other host threads)
+ * race on it and must be serialised by the caller. */
 pi_status pi_sparse_ffn_noalloc(pi_layer *layer, const uint16_t *x, int32_t B,
                                 const int32_t *idx, const int32_t *count, float *y,
                                 void *stream);

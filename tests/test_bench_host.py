@@ -63,3 +63,22 @@ def test_throttle_reasons_are_reported():
     c = _sampler("\n".join(rows)).stop()
     assert c["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
     assert _sampler("").stop() == {"error": "no samples"}
+
+
+def test_hot_concentration():
+    import bench
+    assert bench.hot_concentration([10, 0, 0, 0]) == 0.25        # one neuron carries everything
+    assert bench.hot_concentration([1] * 10) == 0.8               # uniform: 80% of the neurons
+    assert abs(bench.hot_concentration([1, 8, 1]) - 1 / 3) < 1e-12
+    assert bench.hot_concentration([0, 0]) == 0.0
+
+
+def test_auto_replicas_only_for_stacks_that_fit_in_l2():
+    import bench
+    from workload import config_by_name
+    l2 = 129 * 1024 * 1024
+    c1 = config_by_name("opt_layer_d1024")
+    per_layer = 2 * 1024 * 4096 * 2 + bench.predictor_bytes(1024, 4096, 64)
+    R = bench.auto_replicas(c1, 1)
+    assert R * per_layer >= 4 * l2 > (R - 1) * per_layer
+    assert bench.auto_replicas(config_by_name("opt7b_stack"), 32) == 1
