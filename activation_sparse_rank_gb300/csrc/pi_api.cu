@@ -27,14 +27,15 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// dst[k, :] = src[perm[k], :] for rows of `cols` halves (cols % 8 == 0).
+// dst[k, 0:cols] = src[perm[k], :] for rows of `cols` halves (cols % 8 == 0),
+// dst rows dst_ld halves apart; the dst_ld - cols halves after each row are zeroed.
 __global__ void k_permute_rows(const __half *__restrict__ src, __half *__restrict__ dst,
-                               const int32_t *__restrict__ perm, int rows, int cols) {
-  const int nv = cols >> 3;
+                               const int32_t *__restrict__ perm, int rows, int cols, int dst_ld) {
+  const int nv = cols >> 3, nvd = dst_ld >> 3;
   for (int k = blockIdx.x; k < rows; k += gridDim.x) {
     const uint4 *s = reinterpret_cast<const uint4 *>(src + (size_t)perm[k] * cols);
-    uint4 *o = reinterpret_cast<uint4 *>(dst + (size_t)k * cols);
-    for (int v = threadIdx.x; v < nv; v += blockDim.x) o[v] = s[v];
+    uint4 *o = reinterpret_cast<uint4 *>(dst + (size_t)k * dst_ld);
+    for (int v = threadIdx.x; v < nvd; v += blockDim.x) o[v] = v < nv ? s[v] : make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -314,7 +315,8 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   const size_t wrow = (size_t)ffn * d * sizeof(__half);
   size_t off = 0;
   const size_t o_p1 = off; off += align_up((size_t)r * d * sizeof(__half));
-  const size_t o_p2 = off; off += align_up((size_t)ffn * r * sizeof(__half));
+  L->p2_ld = pi::p2_ld_for(r);
+  const size_t o_p2 = off; off += align_up((size_t)ffn * L->p2_ld * sizeof(__half));
   // the gathered rows: fp16, or E4M3 codes (1 byte) plus one scale per row
   const size_t rowmat = q8 ? (size_t)ffn * d : wrow;
   const size_t o_up = off; off += align_up(rowmat);
@@ -373,7 +375,7 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
                                  cudaMemcpyDeviceToDevice, s));
   const int grid_rows = std::min(ffn, 65535);
   k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_p2), L->W_p2,
-                                           perm_dev, ffn, r);
+                                           perm_dev, ffn, r, L->p2_ld);
   // FP8 layers: each permuted fp16 matrix goes through one temporary buffer
   // and is quantised row by row into the layer
   __half *tmp = nullptr;
@@ -393,11 +395,11 @@ pi_status pi_layer_create(pi_layer **out, const pi_layer_desc *D, const int32_t 
   };
   const int grid_q = std::min(ffn, 4 * L->num_sms * 8);
   k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_up), q8 ? tmp : L->W_up,
-                                           perm_dev, ffn, d);
+                                           perm_dev, ffn, d, d);
   if (q8) k_quantize_rows<<<grid_q, 256, 0, s>>>(tmp, L->Q_up, L->s_up, ffn, d);
   if (gated) {
     k_permute_rows<<<grid_rows, 256, 0, s>>>(reinterpret_cast<const __half *>(D->W_gate), q8 ? tmp : L->W_gate,
-                                             perm_dev, ffn, d);
+                                             perm_dev, ffn, d, d);
     if (q8) k_quantize_rows<<<grid_q, 256, 0, s>>>(tmp, L->Q_gate, L->s_gate, ffn, d);
   }
   k_permute_vec<<<(ffn + 255) / 256, 256, 0, s>>>(D->b, L->b, perm_dev, ffn);

@@ -21,7 +21,8 @@ struct pi_layer {
   char *base = nullptr;          // one device allocation holding everything below
   size_t bytes = 0;
   __half *W_p1 = nullptr;        // [rank, d]
-  __half *W_p2 = nullptr;        // [ffn, rank]   permuted rows
+  __half *W_p2 = nullptr;        // [ffn, p2_ld]  permuted rows (rank values, then padding)
+  int p2_ld = 0;                 // elements between stored W_p2 rows
   __half *W_up = nullptr;        // [ffn, d]      permuted rows
   __half *W_gate = nullptr;      // [ffn, d]      permuted rows (ReGLU)
   __half *W_dT = nullptr;        // [ffn, d]      W_down^T, permuted rows
@@ -75,7 +76,7 @@ constexpr int kMaxStack = PI_STACK_LAYERS_PER_LAUNCH;
 
 // Device pointers of one layer, as the persistent kernel sees them.
 struct LayerDev {
-  const __half *W_p1, *W_p2;
+  const __half *W_p1, *W_p2;         // W_p2 rows p2_ld elements apart (StackParams::p2_stride bytes)
   const void *R_up, *R_gate, *R_dT;   // rows: fp16, or E4M3 codes (FP8 layers)
   const float *s_up, *s_gate, *s_dT;  // per-row scales (FP8 layers)
   const float *b, *c_p;
@@ -88,6 +89,7 @@ struct StackParams {
   int G, staged, lanes_l, pf_rows, pf_next;
   int chained;                   // x of layer l > 0 formed from y of layer l - 1
   int lgt_s;                     // log2 threads per staged W_p2 row (logits)
+  int mma_logits, p2_stride;     // staged logits on tensor cores; bytes between staged W_p2 rows
   int off_flag, off_list, off_lb, off_a, off_stage, stage_bytes, slice_pad;   // shared memory layout
   int soff_c, soff_b, soff_p1, soff_p2;                     // offsets inside a stage buffer
   int soff_su, soff_sg, soff_sd;                            // row-scale slices (FP8 layers)
@@ -105,6 +107,11 @@ struct StackParams {
   unsigned *status;
   LayerDev layers[kMaxStack];
 };
+// Stored W_p2 row length in elements: a rank that is a multiple of 64 gets 32
+// elements (64 bytes) of padding per row, so that the decode step's
+// tensor-core logits, which read 16 bytes of 8 consecutive rows at once from
+// a staged copy of the rows, hit distinct shared-memory banks.
+inline int p2_ld_for(int rank) { return rank % 64 == 0 ? rank + 32 : rank; }
 int step_grid(const pi_layer *L);
 int step_slice(const pi_layer *L);
 bool step_staged(const pi_layer *L, int B);

@@ -139,18 +139,20 @@ __device__ unsigned long long g_cta_e[160][16][2];
 // allocation pads both vectors to 256 bytes, so the rounded-up end stays
 // inside it) and, when `with_pred`, its W_p1 rows k = cta, cta+G, ... and
 // its W_p2 slice.
+// Called by lane 0 of one warp.  W_p2 rows are p2_stride bytes apart, in the
+// layer and in the copy alike (the slice is one contiguous bulk copy).
 __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half *x, int nb, bool with_x,
                                             int cta, int G, int d, int r, int s0, int s1, bool with_pred,
-                                            __half *x_s, float *c_s, float *b_s, __half *p1_s,
-                                            __half *p2_s, float *su_s, float *sg_s, float *sd_s,
-                                            uint32_t mbar) {
+                                            int p2_stride, __half *x_s, float *c_s, float *b_s,
+                                            __half *p1_s, unsigned char *p2_s, float *su_s, float *sg_s,
+                                            float *sd_s, uint32_t mbar) {
   // su_s / sg_s / sd_s: the row-scale slices of an FP8 layer (up, gate for
   // ReGLU, down^T), or nullptr
   const int s0a = s0 & ~3;
   const uint32_t cb_bytes = (uint32_t)(((s1 - s0a) + 3) & ~3) * 4u;
   const uint32_t x_bytes = with_x ? (uint32_t)nb * (uint32_t)d * 2u : 0u;
   const uint32_t row_bytes = (uint32_t)d * 2u;
-  const uint32_t p2_bytes = with_pred ? (uint32_t)(s1 - s0) * (uint32_t)r * 2u : 0u;
+  const uint32_t p2_bytes = with_pred ? (uint32_t)(s1 - s0) * (uint32_t)p2_stride : 0u;
   int na = 0;
   if (with_pred)
     for (int k = cta; k < r; k += G) ++na;
@@ -170,7 +172,26 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
   int q = 0;
   for (int k = cta; q < na; k += G, ++q)
     tma_load_1d(p1_s + (size_t)q * d, Ld.W_p1 + (size_t)k * d, row_bytes, mbar);
-  if (p2_bytes) tma_load_1d(p2_s, Ld.W_p2 + (size_t)s0 * r, p2_bytes, mbar);
+  if (p2_bytes)
+    tma_load_1d(p2_s, reinterpret_cast<const unsigned char *>(Ld.W_p2) + (size_t)s0 * p2_stride, p2_bytes, mbar);
+}
+
+// Tensor-core fragment helpers (mma.sync m16n8k16, fp16 inputs, fp32 accumulate).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// (hi, lo) fp16 pair of a binary32 value: hi = fp16(v), lo = fp16(v - hi)
+__device__ __forceinline__ void f32_to_pair(float v, __half &hi, __half &lo) {
+  hi = __float2half_rn(v);
+  lo = __float2half_rn(v - __half2float(hi));
+}
+__device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
+  return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
 }
 
 template <int CPT, int NB, bool REGLU, bool FP8>
@@ -206,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
   const int d = p.d, ffn = p.ffn, r = p.rank, nv = d >> 3;
+  const int p2_ld = p.p2_stride >> 1;                          // elements between W_p2 rows
   const uint32_t row_bytes = (uint32_t)d * 2u;                 // an fp16 row (predictor)
   const uint32_t rrow = FP8 ? (uint32_t)d : row_bytes;          // a gathered up / gate / down row
   unsigned *status = p.status;
@@ -249,9 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   auto stage = [&](int layer) {                  // one thread: issue layer's inputs into its buffer
     unsigned char *bsm = stage_buf(layer & 1);
     stage_layer(p.layers[layer], p.x + (size_t)layer * NB * d, NB, !chained || layer == 0, cta, G, d, r,
-                s0, s1, p.staged != 0, reinterpret_cast<__half *>(bsm), reinterpret_cast<float *>(bsm + p.soff_c),
-                reinterpret_cast<float *>(bsm + p.soff_b), reinterpret_cast<__half *>(bsm + p.soff_p1),
-                reinterpret_cast<__half *>(bsm + p.soff_p2),
+                s0, s1, p.staged != 0, p.p2_stride, reinterpret_cast<__half *>(bsm),
+                reinterpret_cast<float *>(bsm + p.soff_c), reinterpret_cast<float *>(bsm + p.soff_b),
+                reinterpret_cast<__half *>(bsm + p.soff_p1), bsm + p.soff_p2,
                 FP8 ? reinterpret_cast<float *>(bsm + p.soff_su) : nullptr,
                 FP8 && REGLU ? reinterpret_cast<float *>(bsm + p.soff_sg) : nullptr,
                 FP8 ? reinterpret_cast<float *>(bsm + p.soff_sd) : nullptr, mbar0 + 8u * (uint32_t)(layer & 1));
@@ -416,7 +438,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     // issued here by the last warp, which has no logits rows to compute when
     // the slice needs fewer than 16 warps
     if (tid == kIssuer && l + 1 < p.n_layers) stage(l + 1);
-    if (p.staged) {
+    if (p.staged && p.mma_logits) {
+      // W_p2 slice in shared memory (padded rows) on the tensor cores: warp m
+      // takes rows [16m, 16m + 16) as the A tile (m16n8k16, fp16); B holds h
+      // as fp16 pairs, column 2t = hi and 2t + 1 = lo of token t, so that the
+      // logit is D[row][2t] + D[row][2t + 1] (binary32 accumulation).  The k
+      // order is permuted (lane c of a quad reads 8 consecutive elements of a
+      // 32-element block, for two k-steps); A and B use the same permutation.
+      const int g = lane >> 2, c4 = lane & 3;
+      const int ntile = (n_rows + 15) >> 4;
+      const unsigned char *p2b = reinterpret_cast<const unsigned char *>(p2_s);
+      for (int m = wid; m < ntile; m += kWarps) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const unsigned char *ra = p2b + (size_t)(16 * m + g) * p.p2_stride + c4 * 16;
+        const unsigned char *rb = ra + (size_t)8 * p.p2_stride;
+        const int tb = g >> 1;                  // token of this lane's B column (valid when g < 2 NB)
+        for (int sp = 0; sp < (r >> 5); ++sp) {
+          const uint4 wa = *reinterpret_cast<const uint4 *>(ra + sp * 64);
+          const uint4 wb = *reinterpret_cast<const uint4 *>(rb + sp * 64);
+          uint32_t b[4] = {0u, 0u, 0u, 0u};
+          if (g < 2 * NB) {
+            // 8 consecutive h values: elements 0-3 of group 4 sp + c4 in the
+            // first half of h4_s, 4-7 in the second
+            const float4 h0 = h4_s[tb * 2 * nvr + 4 * sp + c4], h1 = h4_s[tb * 2 * nvr + nvr + 4 * sp + c4];
+            const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+            __half pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              __half hi, lo;
+              f32_to_pair(hv[j], hi, lo);
+              pk[j] = (g & 1) ? lo : hi;
+            }
+            b[0] = pack_h2(pk[0], pk[1]); b[1] = pack_h2(pk[2], pk[3]);
+            b[2] = pack_h2(pk[4], pk[5]); b[3] = pack_h2(pk[6], pk[7]);
+          }
+          mma_16816(acc, wa.x, wb.x, wa.y, wb.y, b[0], b[1]);
+          mma_16816(acc, wa.z, wb.z, wa.w, wb.w, b[2], b[3]);
+        }
+        // lane (g, c4) holds D[g][2 c4 + {0,1}] in acc[0..1] and D[g + 8][...]
+        // in acc[2..3]: token c4's hi and lo for rows g and g + 8
+        bool on_a = false, on_b = false;
+        const int row_a = 16 * m + g, row_b = row_a + 8;
+        if (c4 < NB) {
+          on_a = row_a < n_rows && (acc[0] + acc[1]) + c_s[s0 + row_a - s0a] > 0.f;
+          on_b = row_b < n_rows && (acc[2] + acc[3]) + c_s[s0 + row_b - s0a] > 0.f;
+        }
+        if (NB == 2) {                          // union over the two tokens (lanes c4 = 0, 1)
+          on_a |= __shfl_xor_sync(0xffffffffu, on_a ? 1 : 0, 1) != 0;
+          on_b |= __shfl_xor_sync(0xffffffffu, on_b ? 1 : 0, 1) != 0;
+        }
+        if (c4 == 0) {
+          if (row_a < n_rows) flag_s[row_a] = on_a ? 1 : 0;
+          if (row_b < n_rows) flag_s[row_b] = on_b ? 1 : 0;
+        }
+      }
+    } else if (p.staged) {
       // W_p2 slice in shared memory: 2^lgt_s threads per row, each summing
       // r / 8 / 2^lgt_s of the row's 16-byte vectors; a row's visiting order
       // is rotated by its place within the quarter-warp so that the 16-byte
@@ -430,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         if (rb + ((wid * 32) >> lgT) >= n_rows) break;   // no row of this warp in this pass or later
         const int rl = rb + rr;
         const bool valid = rl < n_rows;
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(p2_s + (size_t)(valid ? rl : 0) * r);
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(p2_s + (size_t)(valid ? rl : 0) * p2_ld);
         float a4[NB][4];
 #pragma unroll
         for (int t = 0; t < NB; ++t)
@@ -481,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
           for (int u = 0; u < RU; ++u) {
             const int rl = ((it0 + u) * kWarps + wid) * rows_per_warp + lane / GL;
             if (it0 + u < iters && rl < n_rows)
-              wv[u] = p.staged ? reinterpret_cast<const uint4 *>(p2_s + (size_t)rl * r)[v]
-                               : pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p2 + (size_t)(s0 + rl) * r) + v);
+              wv[u] = p.staged ? reinterpret_cast<const uint4 *>(p2_s + (size_t)rl * p2_ld)[v]
+                               : pidev::ld_stream(reinterpret_cast<const uint4 *>(Ld.W_p2 + (size_t)(s0 + rl) * p2_ld) + v);
             else
               wv[u] = make_uint4(0, 0, 0, 0);
           }
@@ -577,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     if (!p.staged && p.pf_next && l + 1 < p.n_layers && tid == 0) {
       const pi::LayerDev &Ln = p.layers[l + 1];
       for (int k = cta; k < r; k += G) pidev::prefetch_l2_bulk(Ln.W_p1 + (size_t)k * d, row_bytes);
-      const uint32_t p2_bytes = (uint32_t)n_rows * (uint32_t)r * 2u;
-      const char *base = reinterpret_cast<const char *>(Ln.W_p2 + (size_t)s0 * r);
+      const uint32_t p2_bytes = (uint32_t)n_rows * (uint32_t)p.p2_stride;
+      const char *base = reinterpret_cast<const char *>(Ln.W_p2 + (size_t)s0 * p2_ld);
       for (uint32_t o = 0; o < p2_bytes; o += 65536u)
         pidev::prefetch_l2_bulk(base + o, min(65536u, p2_bytes - o));
     }
@@ -937,6 +1013,17 @@ struct SmemPlan {
   size_t base_end;
 };
 
+// The staged logits run on the tensor cores when the rank is a multiple of 64
+// (the stored W_p2 rows are then padded, see pi::p2_ld_for); the staged slice
+// is allocated in whole 16-row tiles (the last tile reads, and ignores, rows
+// past the slice).
+bool mma_logits(const pi_layer *L) { return L->rank % 64 == 0 && L->p2_ld == L->rank + 32; }
+int p2_stride(const pi_layer *L) { return L->p2_ld * 2; }
+size_t p2_rows(const pi_layer *L) {
+  const size_t slice = (size_t)pi::step_slice(L);
+  return mma_logits(L) ? (slice + 15) / 16 * 16 : slice;
+}
+
 SmemPlan smem_plan(const pi_layer *L, int B) {
   const int G = pi::step_grid(L);
   const size_t slice = (size_t)pi::step_slice(L);
@@ -959,7 +1046,7 @@ SmemPlan smem_plan(const pi_layer *L, int B) {
   s.soff_sd = so;    so = align128(so + sc);
   s.stage_small = so;
   s.soff_p1 = so;    so = align128(so + na_max * L->d * 2);
-  s.soff_p2 = so;    so = align128(so + slice * L->rank * 2);
+  s.soff_p2 = so;    so = align128(so + p2_rows(L) * (size_t)p2_stride(L));
   s.stage_full = so;
   return s;
 }
@@ -1016,6 +1103,8 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   int lgt = 0;
   while (lgt < 3 && (step_slice(L0) << (lgt + 1)) <= kThreads && ((L0->rank >> 3) % (2 << lgt)) == 0) ++lgt;
   p.lgt_s = lgt;
+  p.mma_logits = mma_logits(L0) ? 1 : 0;
+  p.p2_stride = p2_stride(L0);
   const int rows_per_neuron = L0->act != PI_ACT_RELU ? 3 : 2;
   // early L2 prefetch of the local active rows: up to ~768 KB of rows per CTA
   const int rb = L0->row_format == PI_ROWS_FP8_E4M3 ? L0->d : 2 * L0->d;   // bytes of a gathered row

@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(128) k_predict_h(const __half *__restrict__ W_
 
 // l[b, i] = W_p2[i, :] . h[b, :] + c_p[i]; mask = l > 0.  G lanes share a row
 // (G = 8, 16 or 32 from the rank), h staged in shared memory per token group.
-__global__ void __launch_bounds__(256) k_predict_l(const __half *__restrict__ W_p2,
+// W_p2 rows are ld elements apart.
+__global__ void __launch_bounds__(256) k_predict_l(const __half *__restrict__ W_p2, int ld,
                                                    const float *__restrict__ c_p,
                                                    const float *__restrict__ h, int B, int r,
                                                    int ffn, int G, uint8_t *__restrict__ mask,
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(256) k_predict_l(const __half *__restrict__ W_
 #pragma unroll
       for (int t = 0; t < kBT; ++t) acc[t] = 0.f;
       if (valid) {
-        const uint4 *w = reinterpret_cast<const uint4 *>(W_p2 + (size_t)row * r);
+        const uint4 *w = reinterpret_cast<const uint4 *>(W_p2 + (size_t)row * ld);
         for (int v = sub; v < nv; v += G) {
           const uint4 wv = pidev::ld_stream(w + v);
           const __half2 *wh = reinterpret_cast<const __half2 *>(&wv);
@@ -219,7 +220,7 @@ cudaError_t run_predict(const pi_layer *L, const __half *x, int B, uint8_t *mask
     e = cudaMemsetAsync(mask, 0, (size_t)L->ffn, s);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(k_predict_l, dim3(grid_l), dim3(256), smem, s, L->W_p2, L->c_p, h_ws, B,
+  return launch_pdl(k_predict_l, dim3(grid_l), dim3(256), smem, s, L->W_p2, L->p2_ld, L->c_p, h_ws, B,
                     L->rank, L->ffn, G, mask, logits, union_mask ? 1 : 0);
 }
 

@@ -229,12 +229,13 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
                                                     const __half *__restrict__ Wu,   // up rows (ReGLU)
                                                     const __grid_constant__ CUtensorMap tm_x,   // B operand
                                                     const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p,
-                                                    int count_const, const float *__restrict__ bias, int d, int ffn,
-                                                    int B, int Bp, int nstage, int kw, __half *__restrict__ abuf,
+                                                    int count_const, const float *__restrict__ bias, int d, int wld,
+                                                    int ffn, int B, int Bp, int nstage, int kw, __half *__restrict__ abuf,
                                                     int abuf_ld, float *__restrict__ piece,
                                                     uint8_t *__restrict__ mask_out, int32_t *__restrict__ tile_cnt,
                                                     unsigned int *status, int silu) {
-  // d: row length of W and contraction length K; ffn: number of rows of W.
+  // d: row length of W and contraction length K; wld: elements between the
+  // rows of W; ffn: number of rows of W.
   // A pipeline stage holds kw consecutive 64-element K slabs, so every
   // gathered row contributes kw * 128 contiguous bytes per stage.
   extern __shared__ __align__(1024) unsigned char smraw[];
@@ -307,8 +308,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
       for (int i = 0; i < 8; ++i) {
         const int q = (tid >> 3) + 16 * i;
         const int rid = rows_s[q] >= 0 ? rows_s[q] : 0;
-        gsrc[i] = Wg + (size_t)rid * d + cch * 8;
-        usrc[i] = REGLU ? Wu + (size_t)rid * d + cch * 8 : nullptr;
+        gsrc[i] = Wg + (size_t)rid * wld + cch * 8;
+        usrc[i] = REGLU ? Wu + (size_t)rid * wld + cch * 8 : nullptr;
       }
       auto issue = [&](int kt, uint32_t g) {
         const int s = (int)(g % (uint32_t)nstage);
@@ -762,7 +763,7 @@ constexpr size_t kTcSmemBudget = 200 * 1024;
 template <int MODE, bool REGLU>
 cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, const CUtensorMap &tm_x,
                         const int32_t *idx, const int32_t *count, int count_const, const float *bias, int K,
-                        int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, float *piece,
+                        int wld, int nrows, int B, int Bp, __half *out, int out_ld, uint8_t *mask, float *piece,
                         int32_t *tile_cnt, bool rows_known, cudaStream_t s, int silu = 0) {
   const int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
@@ -784,7 +785,7 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   auto kern = k_tc_rows<MODE, REGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<G, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, nrows, B, Bp, ns, kw, out, out_ld,
+  kern<<<G, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, wld, nrows, B, Bp, ns, kw, out, out_ld,
                             piece, mask, tile_cnt, L->status, silu);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -829,10 +830,10 @@ cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *m
     return cudaErrorInvalidValue;
   // h = ReLU(W_p1 x) as an fp16 pair, then l = W_p2 h + c_p -> union mask
   // and per-tile counts, then the ordered list of active neurons
-  cudaError_t e = launch_rows<kHidden, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr, L->d,
+  cudaError_t e = launch_rows<kHidden, false>(L, L->W_p1, nullptr, tm_x, nullptr, nullptr, L->rank, nullptr, L->d, L->d,
                                               rpad, B, Bp, hbuf, rpad, nullptr, piece, nullptr, true, s);
   if (e != cudaSuccess) return e;
-  e = launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->ffn, B,
+  e = launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->p2_ld, L->ffn, B,
                                   Bp, nullptr, 0, mask_union, piece, tile_cnt, true, s);
   if (e != cudaSuccess) return e;
   k_compact_tiles<<<(L->ffn + kTile - 1) / kTile, kTile, 0, s>>>(mask_union, tile_cnt, L->ffn, idx, count);
@@ -856,9 +857,9 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
 
   cudaError_t e = record_hook(L->ev_before, s);
   if (e != cudaSuccess) return e;
-  e = reglu ? launch_rows<kAct, true>(L, L->W_gate, L->W_up, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
+  e = reglu ? launch_rows<kAct, true>(L, L->W_gate, L->W_up, tm_x, idx, count, count_const, L->b, L->d, L->d, L->ffn, B,
                                       Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s, silu)
-            : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->ffn, B,
+            : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->d, L->ffn, B,
                                        Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s);
   if (e != cudaSuccess) return e;
 

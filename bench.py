@@ -55,8 +55,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--rows", choices=["fp16", "fp8"], default="fp16",
                     help="storage of the gathered up/gate/down rows (fp8: E4M3 codes, per-row scale)")
-    ap.add_argument("--batch", type=int, default=1,
-                    help="tokens per decode batch (the headline metric is batch 1)")
+    ap.add_argument("--batch", default="1",
+                    help="tokens per decode batch (the headline metric is batch 1); a comma-separated "
+                         "list measures each batch over the same layers, one line each")
     ap.add_argument("--chained", action="store_true",
                     help="time the chained decode step as the main line (x of layer l+1 = "
                          "fp16(y_l / RMS(y_l)) formed on the device)")
@@ -256,7 +257,7 @@ def run_reference(args, cfg):
         return
     spec = cfg.layer
     n_layers = 2
-    Bt = args.batch
+    Bt = int(str(args.batch).split(",")[0])
     L_total = args.layers or cfg.layers
     host_layers = [{k: (v.cpu() if isinstance(v, torch.Tensor) else v)
                     for k, v in make_layer(spec, cfg.seed, l, device="cpu").items()}
@@ -371,255 +372,263 @@ def main():
     spec = cfg.layer
     n_layers = args.layers or cfg.layers
     T = args.tokens or cfg.tokens
-    Bt = args.batch
+    batches = [int(b) for b in str(args.batch).split(",")]
     rows = args.rows
-    if rows == "fp8" and Bt > 2:
+    if rows == "fp8" and max(batches) > 2:
         raise SystemExit("--rows fp8 runs at batch 1 or 2 (the persistent decode step)")
     # the CPU baseline times the fp16 oracle; it belongs to the fp16 workload
-    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1 and Bt == 1 and rows == "fp16"
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1 and 1 in batches and rows == "fp16"
     t_setup = time.perf_counter()
     R = args.replicas or auto_replicas(cfg, n_layers, device)
     layers, host_layers = build_stack(cfg, device, n_layers, keep_host_layers=2 if want_cpu else 0,
                                       rows=rows, replicas=R)
     NL = len(layers)                      # layers one token passes: R copies of the stack
-    stack = SparseFFNStack(layers, tokens=T, B=Bt, chained=args.chained)
-    X = make_tokens(spec.d, T * NL * Bt, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
-    stack.x.copy_(X.view(T, NL, Bt, spec.d))
-    del X
-    stack.build_graph()
-    torch.cuda.synchronize()
-    setup_s = time.perf_counter() - t_setup
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+    def measure(Bt, t_setup):
+        stack = SparseFFNStack(layers, tokens=T, B=Bt, chained=args.chained)
+        X = make_tokens(spec.d, T * NL * Bt, sub_seed(cfg.seed, 1000 + rank, "bench_x"), device)
+        stack.x.copy_(X.view(T, NL, Bt, spec.d))
+        del X
+        stack.build_graph()
+        torch.cuda.synchronize()
+        setup_s = time.perf_counter() - t_setup
+        cpu_here = want_cpu and Bt == 1
 
-    s = stack.stream
-    for _ in range(max(3, args.warmup)):
-        with torch.cuda.stream(s):
-            stack.graph.replay()
-    s.synchronize()
+        def barrier():
+            if world > 1:
+                torch.distributed.barrier()
 
-    clocks = ClockSampler(local)
-    evs_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    barrier()
-    torch.cuda.synchronize()
-    evs_step[0].record(s)
-    with torch.cuda.stream(s):
-        for k in range(args.steps):
-            stack.graph.replay()
-            evs_step[k + 1].record(s)
-    torch.cuda.synchronize()
-    barrier()
-    clk = clocks.stop()
-    step_ms = [evs_step[k].elapsed_time(evs_step[k + 1]) for k in range(args.steps)]
-    ms = max_over_ranks(evs_step[0].elapsed_time(evs_step[-1]) / args.steps, device=device)
-    for layer in layers:
-        if layer.device_status() != 0:
-            raise RuntimeError("device check failed during the timed steps")
-
-    tokens_step = T * Bt * R            # tokens of the n_layers-layer workload per step
-    value = tokens_step * world / (ms / 1000.0)
-    repeats = {"n": len(step_ms), "median_ms": statistics.median(step_ms), "min_ms": min(step_ms),
-               "max_ms": max(step_ms),
-               "median_tokens_per_s": tokens_step * world / (statistics.median(step_ms) / 1000.0),
-               "max_tokens_per_s": tokens_step * world / (min(step_ms) / 1000.0)}
-    tb = touched_bytes(cfg, stack.count, rows)
-    mean_S = float(stack.count.double().mean().item())
-    eff_gbs = tb / (ms / 1000.0) / 1e9
-    peak, peak_kind = measured_peaks()
-    gpu_launches = stack.launches_per_step() * args.steps
-
-    # dense comparator: the same kernels over every neuron, 16 tokens (fp16
-    # rows only: the standalone operators read fp16 rows)
-    dense_tok_s = None
-    if rows == "fp16":
-        Td = min(16, T)
-        dense_g = torch.cuda.CUDAGraph()
-        ws = stack.ws
-        yd = torch.empty(NL, Bt, spec.d, dtype=torch.float32, device=device)
-        with torch.cuda.stream(s):
-            for li, layer in enumerate(layers):
-                layer.dense_ref(stack.x[0, li], yd[li], ws=ws, stream=s)
+        s = stack.stream
+        for _ in range(max(3, args.warmup)):
+            with torch.cuda.stream(s):
+                stack.graph.replay()
         s.synchronize()
-        with torch.cuda.graph(dense_g, stream=s):
-            for t in range(Td):
+
+        clocks = ClockSampler(local)
+        evs_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        barrier()
+        torch.cuda.synchronize()
+        evs_step[0].record(s)
+        with torch.cuda.stream(s):
+            for k in range(args.steps):
+                stack.graph.replay()
+                evs_step[k + 1].record(s)
+        torch.cuda.synchronize()
+        barrier()
+        clk = clocks.stop()
+        step_ms = [evs_step[k].elapsed_time(evs_step[k + 1]) for k in range(args.steps)]
+        ms = max_over_ranks(evs_step[0].elapsed_time(evs_step[-1]) / args.steps, device=device)
+        for layer in layers:
+            if layer.device_status() != 0:
+                raise RuntimeError("device check failed during the timed steps")
+
+        tokens_step = T * Bt * R            # tokens of the n_layers-layer workload per step
+        value = tokens_step * world / (ms / 1000.0)
+        repeats = {"n": len(step_ms), "median_ms": statistics.median(step_ms), "min_ms": min(step_ms),
+                   "max_ms": max(step_ms),
+                   "median_tokens_per_s": tokens_step * world / (statistics.median(step_ms) / 1000.0),
+                   "max_tokens_per_s": tokens_step * world / (min(step_ms) / 1000.0)}
+        tb = touched_bytes(cfg, stack.count, rows)
+        mean_S = float(stack.count.double().mean().item())
+        eff_gbs = tb / (ms / 1000.0) / 1e9
+        peak, peak_kind = measured_peaks()
+        gpu_launches = stack.launches_per_step() * args.steps
+
+        # dense comparator: the same kernels over every neuron, 16 tokens (fp16
+        # rows only: the standalone operators read fp16 rows)
+        dense_tok_s = None
+        if rows == "fp16":
+            Td = min(16, T)
+            dense_g = torch.cuda.CUDAGraph()
+            ws = stack.ws
+            yd = torch.empty(NL, Bt, spec.d, dtype=torch.float32, device=device)
+            with torch.cuda.stream(s):
                 for li, layer in enumerate(layers):
-                    layer.dense_ref(stack.x[t, li], yd[li], ws=ws, stream=s)
-        for _ in range(2):
-            dense_g.replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        with torch.cuda.stream(s):
-            for _ in range(3):
+                    layer.dense_ref(stack.x[0, li], yd[li], ws=ws, stream=s)
+            s.synchronize()
+            with torch.cuda.graph(dense_g, stream=s):
+                for t in range(Td):
+                    for li, layer in enumerate(layers):
+                        layer.dense_ref(stack.x[t, li], yd[li], ws=ws, stream=s)
+            for _ in range(2):
                 dense_g.replay()
-        e1.record(s)
-        torch.cuda.synchronize()
-        dense_tok_s = 3 * Td * Bt * R / (e0.elapsed_time(e1) / 1000.0)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    dense_g.replay()
+            e1.record(s)
+            torch.cuda.synchronize()
+            dense_tok_s = 3 * Td * Bt * R / (e0.elapsed_time(e1) / 1000.0)
 
-    # dominant kernel (the persistent step kernel, one launch per token)
-    # timed inside a captured step with external event-record nodes
-    Tr = min(64, T)
-    try:
-        evs = {t: (torch.cuda.Event(enable_timing=True, external=True),
-                   torch.cuda.Event(enable_timing=True, external=True)) for t in range(Tr)}
-        how = "external event-record nodes around each launch inside a captured step"
-    except TypeError:
-        evs = None
-        how = None
-    if evs is not None:
-        for a, b in evs.values():      # materialise the events before capture
-            a.record(s); b.record(s)
-        s.synchronize()
-        g_inst = stack.capture(timing_events=evs, tokens=Tr)
-        with torch.cuda.stream(s):
-            g_inst.replay()
-        s.synchronize()
-    else:
-        evs = {t: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for t in range(Tr)}
-        with torch.cuda.stream(s):
-            for t in range(Tr):
-                layers[0].set_timing_events(*evs[t])
-                stack._token(t, s)
-                layers[0].set_timing_events(None, None)
-        s.synchronize()
-        how = "events around each launch, eager step"
-    k_ms = [evs[t][0].elapsed_time(evs[t][1]) for t in range(Tr)]
-    cnt = stack.count[:Tr].cpu().numpy()
-    # layers[0]'s timing hook brackets the launch that holds layer 0: the first
-    # PI_STACK_LAYERS_PER_LAUNCH layers of a longer stack
-    L1 = min(NL, pi.PI_STACK_LAYERS_PER_LAUNCH)
-    if Bt <= 2:   # the persistent step: predictor + rows of the launch's layers
-        alg_bytes = (Tr * L1 * predictor_bytes(spec.d, spec.ffn, spec.rank)
-                     + float(cnt[:, :L1].sum()) * bytes_per_active_neuron(spec.d, spec.act, rows))
-        kname = f"k_stack_step (one token through {L1} layers)"
-    else:         # tensor-core up + down of layer 0: its active rows
-        alg_bytes = float(cnt[:, 0].sum()) * bytes_per_active_neuron(spec.d, spec.act)
-        kname = "k_tc_rows<act> + k_tc_down (layer 0, tcgen05)"
-    k_avg_ms = sum(k_ms) / len(k_ms)
-    achieved = alg_bytes / len(k_ms) / (k_avg_ms / 1e3) / 1e9
-    traffic = None
-    tfile = ROOT / "profiles" / "stack_step_traffic.json"
-    if tfile.exists():
-        tj = json.loads(tfile.read_text())
-        # counters of this kernel on this workload's layers, per layer
-        if tj.get("kernel_source_hash") == kernel_source_hash() and tj.get("config") == cfg.name:
-            traffic = tj["bytes_per_layer"] * L1
-    if Bt > 2 or rows != "fp16":     # the stored counters are of the fp16 step kernel
+        # dominant kernel (the persistent step kernel, one launch per token)
+        # timed inside a captured step with external event-record nodes
+        Tr = min(64, T)
+        try:
+            evs = {t: (torch.cuda.Event(enable_timing=True, external=True),
+                       torch.cuda.Event(enable_timing=True, external=True)) for t in range(Tr)}
+            how = "external event-record nodes around each launch inside a captured step"
+        except TypeError:
+            evs = None
+            how = None
+        if evs is not None:
+            for a, b in evs.values():      # materialise the events before capture
+                a.record(s); b.record(s)
+            s.synchronize()
+            g_inst = stack.capture(timing_events=evs, tokens=Tr)
+            with torch.cuda.stream(s):
+                g_inst.replay()
+            s.synchronize()
+        else:
+            evs = {t: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for t in range(Tr)}
+            with torch.cuda.stream(s):
+                for t in range(Tr):
+                    layers[0].set_timing_events(*evs[t])
+                    stack._token(t, s)
+                    layers[0].set_timing_events(None, None)
+            s.synchronize()
+            how = "events around each launch, eager step"
+        k_ms = [evs[t][0].elapsed_time(evs[t][1]) for t in range(Tr)]
+        cnt = stack.count[:Tr].cpu().numpy()
+        # layers[0]'s timing hook brackets the launch that holds layer 0: the first
+        # PI_STACK_LAYERS_PER_LAUNCH layers of a longer stack
+        L1 = min(NL, pi.PI_STACK_LAYERS_PER_LAUNCH)
+        if Bt <= 2:   # the persistent step: predictor + rows of the launch's layers
+            alg_bytes = (Tr * L1 * predictor_bytes(spec.d, spec.ffn, spec.rank)
+                         + float(cnt[:, :L1].sum()) * bytes_per_active_neuron(spec.d, spec.act, rows))
+            kname = f"k_stack_step (one token through {L1} layers)"
+        else:         # tensor-core up + down of layer 0: its active rows
+            alg_bytes = float(cnt[:, 0].sum()) * bytes_per_active_neuron(spec.d, spec.act)
+            kname = "k_tc_rows<act> + k_tc_down (layer 0, tcgen05)"
+        k_avg_ms = sum(k_ms) / len(k_ms)
+        achieved = alg_bytes / len(k_ms) / (k_avg_ms / 1e3) / 1e9
         traffic = None
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "kernel": kname,
-                "peak_kind": peak_kind + " (copy bandwidth)",
-                "launches_timed": len(k_ms), "avg_launch_us": k_avg_ms * 1e3,
-                "algorithmic_bytes_per_launch": alg_bytes / len(k_ms),
-                "timing": how}
-    if Bt > 2:
-        mult = 3 if spec.act in ("reglu", "swiglu") else 2
-        flops = 2.0 * Bt * float(cnt[:, 0].sum()) * spec.d * mult / len(k_ms)
-        roofline["tensor_tflops"] = flops / (k_avg_ms / 1e3) / 1e12
+        tfile = ROOT / "profiles" / "stack_step_traffic.json"
+        if tfile.exists():
+            tj = json.loads(tfile.read_text())
+            # counters of this kernel on this workload's layers, per layer
+            if tj.get("kernel_source_hash") == kernel_source_hash() and tj.get("config") == cfg.name:
+                traffic = tj["bytes_per_layer"] * L1
+        if Bt > 2 or rows != "fp16":     # the stored counters are of the fp16 step kernel
+            traffic = None
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "kernel": kname,
+                    "peak_kind": peak_kind + " (copy bandwidth)",
+                    "launches_timed": len(k_ms), "avg_launch_us": k_avg_ms * 1e3,
+                    "algorithmic_bytes_per_launch": alg_bytes / len(k_ms),
+                    "timing": how}
+        if Bt > 2:
+            mult = 3 if spec.act in ("reglu", "swiglu") else 2
+            flops = 2.0 * Bt * float(cnt[:, 0].sum()) * spec.d * mult / len(k_ms)
+            roofline["tensor_tflops"] = flops / (k_avg_ms / 1e3) / 1e12
 
-    # end to end from pinned host buffers through the public API
-    xh = torch.empty_like(stack.x, device="cpu").pin_memory()
-    xh.copy_(stack.x)
-    yh = torch.empty_like(stack.y, device="cpu").pin_memory()
-    for _ in range(2):
-        stack.run_host(xh, yh, stream=s)
-    s.synchronize()
-    E = max(3, min(args.steps, 5))
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(s)
-    for _ in range(E):
-        stack.run_host(xh, yh, stream=s)
-    f1.record(s)
-    s.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / E
-    e2e = {"value": tokens_step * world / (e2e_ms / 1000.0), "unit": "tokens/s",
-           "h2d_bytes_per_step": xh.numel() * xh.element_size(),
-           "d2h_bytes_per_step": yh.numel() * yh.element_size()}
-
-    # the same step with each layer's input formed from the previous layer's
-    # output on the device (a decoder's dependence), beside the main line
-    chained_line = None
-    if not args.chained and not args.no_chained_line:
-        cst = SparseFFNStack(layers, tokens=T, B=Bt, chained=True)
-        cst.x[:, 0].copy_(stack.x[:, 0])
-        cst.build_graph()
+        # end to end from pinned host buffers through the public API
+        xh = torch.empty_like(stack.x, device="cpu").pin_memory()
+        xh.copy_(stack.x)
+        yh = torch.empty_like(stack.y, device="cpu").pin_memory()
         for _ in range(2):
+            stack.run_host(xh, yh, stream=s)
+        s.synchronize()
+        E = max(3, min(args.steps, 5))
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(s)
+        for _ in range(E):
+            stack.run_host(xh, yh, stream=s)
+        f1.record(s)
+        s.synchronize()
+        e2e_ms = f0.elapsed_time(f1) / E
+        e2e = {"value": tokens_step * world / (e2e_ms / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+               "d2h_bytes_per_step": yh.numel() * yh.element_size()}
+
+        # the same step with each layer's input formed from the previous layer's
+        # output on the device (a decoder's dependence), beside the main line
+        chained_line = None
+        if not args.chained and not args.no_chained_line:
+            cst = SparseFFNStack(layers, tokens=T, B=Bt, chained=True)
+            cst.x[:, 0].copy_(stack.x[:, 0])
+            cst.build_graph()
+            for _ in range(2):
+                with torch.cuda.stream(cst.stream):
+                    cst.graph.replay()
+            cst.stream.synchronize()
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            Kc = max(3, min(args.steps, 5))
+            c0.record(cst.stream)
             with torch.cuda.stream(cst.stream):
-                cst.graph.replay()
-        cst.stream.synchronize()
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        Kc = max(3, min(args.steps, 5))
-        c0.record(cst.stream)
-        with torch.cuda.stream(cst.stream):
-            for _ in range(Kc):
-                cst.graph.replay()
-        c1.record(cst.stream)
-        cst.stream.synchronize()
-        c_ms = c0.elapsed_time(c1) / Kc
-        c_tb = touched_bytes(cfg, cst.count, rows)
-        chained_line = {"value": tokens_step * world / (c_ms / 1000.0), "unit": "tokens/s",
-                        "ms_per_step": c_ms, "effective_hbm_gbs": c_tb / (c_ms / 1000.0) / 1e9,
-                        "mean_active": float(cst.count.double().mean().item()),
-                        "what": "x of layer l+1 = fp16(y_l / RMS(y_l)) formed on the device after "
-                                "layer l completes; only layer 0's x is an input"}
-        del cst
+                for _ in range(Kc):
+                    cst.graph.replay()
+            c1.record(cst.stream)
+            cst.stream.synchronize()
+            c_ms = c0.elapsed_time(c1) / Kc
+            c_tb = touched_bytes(cfg, cst.count, rows)
+            chained_line = {"value": tokens_step * world / (c_ms / 1000.0), "unit": "tokens/s",
+                            "ms_per_step": c_ms, "effective_hbm_gbs": c_tb / (c_ms / 1000.0) / 1e9,
+                            "mean_active": float(cst.count.double().mean().item()),
+                            "what": "x of layer l+1 = fp16(y_l / RMS(y_l)) formed on the device after "
+                                    "layer l completes; only layer 0's x is an input"}
+            del cst
 
-    # with copies, the same step over one copy (its weights may stay in L2)
-    warm = None
-    if R > 1:
-        st1 = SparseFFNStack(layers[:n_layers], tokens=T, B=Bt)
-        st1.x.copy_(stack.x[:, :n_layers])
-        st1.build_graph()
-        for _ in range(3):
+        # with copies, the same step over one copy (its weights may stay in L2)
+        warm = None
+        if R > 1:
+            st1 = SparseFFNStack(layers[:n_layers], tokens=T, B=Bt)
+            st1.x.copy_(stack.x[:, :n_layers])
+            st1.build_graph()
+            for _ in range(3):
+                with torch.cuda.stream(st1.stream):
+                    st1.graph.replay()
+            st1.stream.synchronize()
+            w0 = torch.cuda.Event(enable_timing=True)
+            w1 = torch.cuda.Event(enable_timing=True)
+            w0.record(st1.stream)
             with torch.cuda.stream(st1.stream):
-                st1.graph.replay()
-        st1.stream.synchronize()
-        w0 = torch.cuda.Event(enable_timing=True)
-        w1 = torch.cuda.Event(enable_timing=True)
-        w0.record(st1.stream)
-        with torch.cuda.stream(st1.stream):
-            for _ in range(5):
-                st1.graph.replay()
-        w1.record(st1.stream)
-        st1.stream.synchronize()
-        warm = {"value": 5 * T * Bt / (w0.elapsed_time(w1) / 1000.0), "unit": "tokens/s",
-                "what": "one copy of the stack, replayed: its weights can stay in L2"}
-        del st1
-    concentration = profile_concentration(cfg, device)
+                for _ in range(5):
+                    st1.graph.replay()
+            w1.record(st1.stream)
+            st1.stream.synchronize()
+            warm = {"value": 5 * T * Bt / (w0.elapsed_time(w1) / 1000.0), "unit": "tokens/s",
+                    "what": "one copy of the stack, replayed: its weights can stay in L2"}
+            del st1
+        concentration = profile_concentration(cfg, device)
 
-    cpu = None
-    if want_cpu:
-        xh_l = stack.x[:, :2].cpu()
-        v, sample = time_oracle(host_layers, xh_l, n_layers, args.cpu_seconds)
-        cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": sample + f"; scaled to a {n_layers}-layer stack; numpy float64, default BLAS threads"}
+        cpu = None
+        if cpu_here:
+            xh_l = stack.x[:, :2].cpu()
+            v, sample = time_oracle(host_layers, xh_l, n_layers, args.cpu_seconds)
+            cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": sample + f"; scaled to a {n_layers}-layer stack; numpy float64, default BLAS threads"}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
-            "config": workload_config(cfg, n_layers, T, Bt, world, rows, args.chained, R),
-            "effective_hbm_gbs": eff_gbs,
-            "effective_frac_of_measured": eff_gbs / peak,
-            "effective_frac_of_nominal_8tbs": eff_gbs / (NOMINAL_HBM_GBS),
-            "touched_bytes_per_step": tb, "mean_active": mean_S,
-            "dense_tokens_per_s": dense_tok_s,
-            "speedup_vs_dense": value / world / dense_tok_s if dense_tok_s else None,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "chained_decode": chained_line,
-            "repeats": repeats, "warm_l2": warm, "hot_concentration": concentration,
-            "gpu_launches": gpu_launches, "clocks": clk, "setup_s": setup_s,
-        }
-        print(json.dumps(line), flush=True)
+        if rank == 0:
+            line = {
+                "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": workload_config(cfg, n_layers, T, Bt, world, rows, args.chained, R),
+                "effective_hbm_gbs": eff_gbs,
+                "effective_frac_of_measured": eff_gbs / peak,
+                "effective_frac_of_nominal_8tbs": eff_gbs / (NOMINAL_HBM_GBS),
+                "touched_bytes_per_step": tb, "mean_active": mean_S,
+                "dense_tokens_per_s": dense_tok_s,
+                "speedup_vs_dense": value / world / dense_tok_s if dense_tok_s else None,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "chained_decode": chained_line,
+                "repeats": repeats, "warm_l2": warm, "hot_concentration": concentration,
+                "gpu_launches": gpu_launches, "clocks": clk, "setup_s": setup_s,
+            }
+            print(json.dumps(line), flush=True)
+
+    for Bt in batches:
+        measure(Bt, t_setup)
+        t_setup = time.perf_counter()
+
     if world > 1:
         torch.distributed.destroy_process_group()
 

@@ -264,14 +264,16 @@ def preact_error_bound(L: OracleLayer, x) -> np.ndarray:
 
 
 def predicted_forward(L: OracleLayer, x) -> Dict[str, np.ndarray]:
-    """The whole path for one batch: predictor, union set, sparse FFN."""
+    """The whole path for one batch: predictor, union set, sparse FFN.
+    tau is the band of the bound's fp16-pair form (split=True), which also
+    covers the plain binary32 form: a GPU may compute the logits either way."""
     x = _f64(x).reshape(-1, L.d)
     h = predictor_hidden(L, x)
     l = predictor_logits(L, h)
     mask = predicted_mask(l)
     S = active_union(mask)
     y = sparse_ffn(L, x, S)
-    return dict(h=h, l=l, mask=mask, S=S, y=y, tau=logit_error_bound(L, x, h))
+    return dict(h=h, l=l, mask=mask, S=S, y=y, tau=logit_error_bound(L, x, h, split=True))
 
 
 # --------------------------------------------------------------------------

@@ -1,7 +1,9 @@
-"""The decode step's logits at slice shapes that choose the other thread
-layouts of the staged W_p2 block: two threads per row (slices of 129-256
-neurons, or r / 8 not a multiple of 4) and one thread per row over two passes
-of the CTA (slices of more than 512 neurons), against the float64 oracle."""
+"""The decode step's logits at slice shapes that choose each form of the
+staged W_p2 block: on the tensor cores (rank a multiple of 64; 200-neuron
+slices, and 300-neuron slices that need more 16-row tiles than the CTA has
+warps), and on the ALU where the rank is not a multiple of 64 (r / 8 = 6: two
+threads per row, three vectors each; 527-neuron slices: one thread per row
+over two passes of the CTA), against the float64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -22,7 +24,8 @@ def pi():
 
 
 @pytest.mark.parametrize("act,d,ffn,r", [
-    ("relu", 1024, 30400, 64),    # 200-neuron slices on 152 SMs: two threads per row
+    ("relu", 1024, 30400, 64),    # 200-neuron slices on 152 SMs: 13 row tiles on the tensor cores
+    ("relu", 512, 45600, 64),     # 300-neuron slices: 19 row tiles, more than the CTA's 16 warps
     ("reglu", 512, 4096, 48),     # r / 8 = 6: two threads per row, three vectors each
     ("relu", 256, 80000, 16),     # 527-neuron slices: one thread per row, two passes
 ])
