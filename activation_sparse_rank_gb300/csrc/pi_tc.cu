@@ -271,6 +271,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = taddr_s;
+  // the set-up above overlaps the previous kernel's tail (programmatic
+  // dependent launch); nothing it writes or reads is touched before this
+  pidev::griddep_wait();
+  pidev::griddep_launch();
 
   int count = count_p ? *count_p : count_const;
   if (count < 0 || count > ffn) {
@@ -416,6 +420,8 @@ __global__ void __launch_bounds__(1024) k_tc_fixup(const float *__restrict__ pie
                                                    int grid, __half *__restrict__ abuf, int abuf_ld,
                                                    uint8_t *__restrict__ mask_out, int32_t *__restrict__ tile_cnt,
                                                    unsigned int *status, int silu) {
+  pidev::griddep_wait();
+  pidev::griddep_launch();
   constexpr int NA = REGLU ? 2 : 1;
   const int Nmma = MODE == kLogits ? 2 * Bp : Bp;
   const int ncolD = NA * Nmma;
@@ -498,6 +504,8 @@ __global__ void __launch_bounds__(kTile) k_compact_tiles(const uint8_t *__restri
                                                          int32_t *__restrict__ idx, int32_t *__restrict__ count) {
   __shared__ int red_s[4];
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  pidev::griddep_wait();
+  pidev::griddep_launch();
   int pre = 0;
   for (int k = tid; k < t; k += kTile) pre += tile_cnt[k];
 #pragma unroll
@@ -562,6 +570,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = taddr_s;
+  pidev::griddep_wait();
+  pidev::griddep_launch();
 
   int count = count_p ? *count_p : count_const;
   if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;     // flagged by the up kernel
@@ -691,6 +701,8 @@ __global__ void __launch_bounds__(512) k_tc_down_reduce(const float *__restrict_
   __shared__ int slots_s[2 * kCtasPerTile + 4];
   __shared__ int nslot_s;
   const int tile = blockIdx.x, b = blockIdx.y;
+  pidev::griddep_wait();
+  pidev::griddep_launch();
   int count = count_p ? *count_p : count_const;
   if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;
   const long long KS = (count + kSlab - 1) / kSlab;
@@ -785,14 +797,12 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   auto kern = k_tc_rows<MODE, REGLU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<G, 128, smem, s>>>(Wg, Wu, tm_x, idx, count, count_const, bias, K, wld, nrows, B, Bp, ns, kw, out, out_ld,
-                            piece, mask, tile_cnt, L->status, silu);
-  e = cudaGetLastError();
+  e = pi::launch_pdl(kern, dim3(G), dim3(128), smem, s, Wg, Wu, tm_x, idx, count, count_const, bias, K, wld, nrows,
+                     B, Bp, ns, kw, out, out_ld, piece, mask, tile_cnt, L->status, silu);
   if (e != cudaSuccess) return e;
   const int groups = std::min(Bp / 8, 8);       // 128 threads per group of token columns
-  k_tc_fixup<MODE, REGLU><<<G, kTile * groups, 0, s>>>(piece, idx, count, count_const, bias, nrows, B, Bp,
-                                                       slabs / kw, G, out, out_ld, mask, tile_cnt, L->status, silu);
-  return cudaGetLastError();
+  return pi::launch_pdl(k_tc_fixup<MODE, REGLU>, dim3(G), dim3(kTile * groups), 0, s, piece, idx, count, count_const,
+                        bias, nrows, B, Bp, slabs / kw, G, out, out_ld, mask, tile_cnt, L->status, silu);
 }
 
 }  // namespace
@@ -836,8 +846,8 @@ cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *m
   e = launch_rows<kLogits, false>(L, L->W_p2, nullptr, tm_h, nullptr, nullptr, L->ffn, L->c_p, L->rank, L->p2_ld, L->ffn, B,
                                   Bp, nullptr, 0, mask_union, piece, tile_cnt, true, s);
   if (e != cudaSuccess) return e;
-  k_compact_tiles<<<(L->ffn + kTile - 1) / kTile, kTile, 0, s>>>(mask_union, tile_cnt, L->ffn, idx, count);
-  return cudaGetLastError();
+  return launch_pdl(k_compact_tiles, dim3((L->ffn + kTile - 1) / kTile), dim3(kTile), 0, s, mask_union, tile_cnt,
+                    L->ffn, idx, count);
 }
 
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
@@ -873,16 +883,14 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   const size_t dn_smem = 1024 + dn_ns * dn_stage;
   e = cudaFuncSetAttribute(k_tc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
   if (e != cudaSuccess) return e;
-  k_tc_down<<<L->num_sms, 128, dn_smem, s>>>(L->W_dT, tm_a, idx, count, count_const, L->d, L->ffn, B, Bp, dn_ns,
-                                             cw, piece, L->status);
-  e = cudaGetLastError();
+  e = launch_pdl(k_tc_down, dim3(L->num_sms), dim3(128), dn_smem, s, L->W_dT, tm_a, idx, count, count_const, L->d,
+                 L->ffn, B, Bp, dn_ns, cw, piece, L->status);
   if (e != cudaSuccess) return e;
   e = record_hook(L->ev_after, s);
   if (e != cudaSuccess) return e;
   const int CW = cw * kTile;
-  k_tc_down_reduce<<<dim3((L->d + CW - 1) / CW, B), CW, 0, s>>>(piece, count, count_const, L->d, L->ffn, B, CW,
-                                                                L->num_sms, y);
-  return cudaGetLastError();
+  return launch_pdl(k_tc_down_reduce, dim3((L->d + CW - 1) / CW, B), dim3(CW), 0, s, piece, count, count_const, L->d,
+                    L->ffn, B, CW, L->num_sms, y);
 }
 
 }  // namespace pi
