@@ -562,7 +562,12 @@ pi_status pi_layer_forward(pi_layer *L, const uint16_t *x, int32_t B, int32_t *i
   st = need_fp16_rows(L, "pi_layer_forward with more than 2 tokens");
   if (st != PI_OK) return st;
   uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
-  if (pi::tc_predict_supported(L, B)) {
+  if (pi::pbatch_supported(L, B)) {
+    PI_TRY_CUDA(pi::run_predict_batch(L, xh, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
+                                       reinterpret_cast<float *>(wsb + w.tcpart),
+                                       reinterpret_cast<int32_t *>(wsb + w.cnt),
+                                       reinterpret_cast<unsigned *>(wsb + w.bar), idx, count, s));
+  } else if (pi::tc_predict_supported(L, B)) {
     PI_TRY_CUDA(pi::run_predict_tc(L, xh, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
                                     reinterpret_cast<float *>(wsb + w.tcpart),
                                     reinterpret_cast<int32_t *>(wsb + w.tcnt), idx, count, s));
@@ -639,7 +644,13 @@ pi_status stack_forward_impl(pi_layer *const *layers, int32_t n_layers, uint16_t
   for (int l = 0; l < n_layers; ++l) {
     pi_layer *Ll = layers[l];
     uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
-    if (pi::tc_predict_supported(Ll, B)) {
+    if (pi::pbatch_supported(Ll, B)) {
+      PI_TRY_CUDA(pi::run_predict_batch(Ll, xh + l * xs, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
+                                         reinterpret_cast<float *>(wsb + w.tcpart),
+                                         reinterpret_cast<int32_t *>(wsb + w.cnt),
+                                         reinterpret_cast<unsigned *>(wsb + w.bar), idx + (size_t)l * L->ffn,
+                                         count + l, s));
+    } else if (pi::tc_predict_supported(Ll, B)) {
       PI_TRY_CUDA(pi::run_predict_tc(Ll, xh + l * xs, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
                                       reinterpret_cast<float *>(wsb + w.tcpart),
                                       reinterpret_cast<int32_t *>(wsb + w.tcnt), idx + (size_t)l * L->ffn,
@@ -748,14 +759,14 @@ pi_status pi_layer_set_hot_count(pi_layer *L, int32_t n_hot) {
 int32_t pi_forward_launches(const pi_layer *L, int32_t B) {
   if (!L || B < 1 || B > PI_MAX_BATCH) return 0;
   // B <= 2: the persistent step and the ordered compaction of its masks
-  // (memsets not counted).  Otherwise, on the tensor cores: hidden layer and
-  // logits (each with its split-tile fix-up), tile compaction, up (+ fix-up),
-  // down, column reduce; the predictor on the ALU instead: predict_h,
-  // predict_l, compact; without tensor cores: predictor, compact, up, down,
-  // reduce.
+  // (memsets not counted).  Otherwise the predictor, then the FFN.  The
+  // predictor: one cooperative launch (B <= 32, pi_pbatch.cu); else on the
+  // tensor cores hidden layer and logits (each with its split-tile fix-up)
+  // and tile compaction; else predict_h, predict_l, compact.  The FFN on the
+  // tensor cores: up (+ fix-up), down, column reduce; else up, down, reduce.
   if (B <= 2) return 2;
-  if (!pi::tc_supported(L, B)) return 6;
-  return pi::tc_predict_supported(L, B) ? 9 : 7;
+  const int pred = pi::pbatch_supported(L, B) ? 1 : (pi::tc_predict_supported(L, B) ? 5 : 3);
+  return pred + (pi::tc_supported(L, B) ? 4 : 3);
 }
 
 pi_status pi_device_status(pi_layer *L, void *stream) {

@@ -173,6 +173,13 @@ int tc_rank_pad(const pi_layer *L);
 cudaError_t run_predict_tc(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
                            float *piece, int32_t *tile_cnt, int32_t *idx, int32_t *count, cudaStream_t s);
 size_t tc_piece_bytes(const pi_layer *L, int B);
+// The same predictor (hbuf as [2B, rank], the union mask, idx / count) in one
+// cooperative launch for 3 <= B <= 32 (pi_pbatch.cu); partial: fp32 scratch
+// of tc_piece_bytes; cnt: int [num_sms]; bar: a grid-barrier counter.
+bool pbatch_supported(const pi_layer *L, int B);
+cudaError_t run_predict_batch(const pi_layer *L, const __half *x, int B, uint8_t *mask_union, __half *hbuf,
+                              float *partial, int32_t *cnt, unsigned *bar, int32_t *idx, int32_t *count,
+                              cudaStream_t s);
 cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                               const int32_t *count, int count_const, float *y, const WsLayout &w,
                               char *ws, cudaStream_t s);
