@@ -478,14 +478,6 @@ static pi_status check_common(const pi_layer *L, const uint16_t *x, int32_t B, c
   return PI_OK;
 }
 
-// Entry points that read fp16 rows (the standalone sparse operators and the
-// tensor-core path) do not take FP8 layers.
-static pi_status need_fp16_rows(const pi_layer *L, const char *what) {
-  if (L->row_format != PI_ROWS_FP16)
-    return pi::fail(PI_ERR_UNSUPPORTED, "%s needs a layer with fp16 rows (this one stores FP8 E4M3 rows)", what);
-  return PI_OK;
-}
-
 pi_status pi_predict(pi_layer *L, const uint16_t *x, int32_t B, uint8_t *mask, float *logits,
                      void *ws, size_t ws_bytes, void *stream) {
   g_err[0] = 0;
@@ -521,8 +513,6 @@ pi_status pi_sparse_ffn(pi_layer *L, const uint16_t *x, int32_t B, const int32_t
   if (!idx || !count || !aligned4(idx) || !aligned4(count))
     return pi::fail(PI_ERR_INVALID_ARG, "idx and count must be non-NULL and 4-byte aligned");
   if (!y || !aligned16(y)) return pi::fail(PI_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
-  st = need_fp16_rows(L, "pi_sparse_ffn");
-  if (st != PI_OK) return st;
   PI_TRY_CUDA(pi::run_sparse_ffn(L, reinterpret_cast<const __half *>(x), B, idx, count, 0, y, w,
                                  static_cast<char *>(ws), static_cast<cudaStream_t>(stream)));
   return PI_OK;
@@ -535,8 +525,6 @@ pi_status pi_ffn_dense_ref(pi_layer *L, const uint16_t *x, int32_t B, float *y, 
   pi_status st = check_common(L, x, B, ws, ws_bytes, &w);
   if (st != PI_OK) return st;
   if (!y || !aligned16(y)) return pi::fail(PI_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
-  st = need_fp16_rows(L, "pi_ffn_dense_ref");
-  if (st != PI_OK) return st;
   PI_TRY_CUDA(pi::run_sparse_ffn(L, reinterpret_cast<const __half *>(x), B, nullptr, nullptr,
                                  L->ffn, y, w, static_cast<char *>(ws),
                                  static_cast<cudaStream_t>(stream)));
@@ -559,8 +547,6 @@ pi_status pi_layer_forward(pi_layer *L, const uint16_t *x, int32_t B, int32_t *i
     PI_TRY_CUDA(pi::run_stack(&L, 1, xh, B, idx, count, y, w, wsb, s));
     return PI_OK;
   }
-  st = need_fp16_rows(L, "pi_layer_forward with more than 2 tokens");
-  if (st != PI_OK) return st;
   uint8_t *mask = reinterpret_cast<uint8_t *>(wsb + w.mask);
   if (pi::pbatch_supported(L, B)) {
     PI_TRY_CUDA(pi::run_predict_batch(L, xh, B, mask, reinterpret_cast<__half *>(wsb + w.hbuf),
@@ -602,8 +588,7 @@ __global__ void __launch_bounds__(256) k_chain_x(const float *__restrict__ y, __
 
 pi_status stack_forward_impl(pi_layer *const *layers, int32_t n_layers, uint16_t *x_mut,
                              const uint16_t *x, int32_t B, int32_t *idx, int32_t *count, float *y,
-                             void *ws, size_t ws_bytes, void *stream, bool chained,
-                             const char *where) {
+                             void *ws, size_t ws_bytes, void *stream, bool chained) {
   if (!layers || n_layers < 1) return pi::fail(PI_ERR_INVALID_ARG, "layers is NULL or n_layers < 1");
   for (int l = 0; l < n_layers; ++l) {
     const pi_layer *Ll = layers[l];
@@ -638,8 +623,6 @@ pi_status stack_forward_impl(pi_layer *const *layers, int32_t n_layers, uint16_t
     }
     return PI_OK;
   }
-  st = need_fp16_rows(L, where);
-  if (st != PI_OK) return st;
 
   for (int l = 0; l < n_layers; ++l) {
     pi_layer *Ll = layers[l];
@@ -678,15 +661,14 @@ pi_status pi_stack_forward(pi_layer *const *layers, int32_t n_layers, const uint
                            size_t ws_bytes, void *stream) {
   g_err[0] = 0;
   return stack_forward_impl(layers, n_layers, nullptr, x, B, idx, count, y, ws, ws_bytes, stream,
-                            false, "pi_stack_forward with more than 2 tokens");
+                            false);
 }
 
 pi_status pi_stack_forward_chained(pi_layer *const *layers, int32_t n_layers, uint16_t *x,
                                    int32_t B, int32_t *idx, int32_t *count, float *y, void *ws,
                                    size_t ws_bytes, void *stream) {
   g_err[0] = 0;
-  return stack_forward_impl(layers, n_layers, x, x, B, idx, count, y, ws, ws_bytes, stream, true,
-                            "pi_stack_forward_chained with more than 2 tokens");
+  return stack_forward_impl(layers, n_layers, x, x, B, idx, count, y, ws, ws_bytes, stream, true);
 }
 
 pi_status pi_stack_forward_host(pi_layer *const *layers, int32_t n_layers, int32_t T,
@@ -706,8 +688,7 @@ pi_status pi_stack_forward_host(pi_layer *const *layers, int32_t n_layers, int32
   for (int t = 0; t < T; ++t) {
     uint16_t *xt = x_dev + per_tok * t;
     const pi_status st = stack_forward_impl(layers, n_layers, xt, xt, B, idx, count ? count + (size_t)t * n_layers : nullptr,
-                                            y_dev + per_tok * t, ws, ws_bytes, stream, chained != 0,
-                                            "pi_stack_forward_host with more than 2 tokens");
+                                            y_dev + per_tok * t, ws, ws_bytes, stream, chained != 0);
     if (st != PI_OK) return st;
   }
   PI_TRY_CUDA(cudaMemcpyAsync(y_host, y_dev, sizeof(float) * per_tok * T, cudaMemcpyDeviceToHost, s));

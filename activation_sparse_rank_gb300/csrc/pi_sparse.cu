@@ -208,11 +208,13 @@ __global__ void __launch_bounds__(512) k_fused_small(
 // Generic batch: up kernel writes a[b, k] (by list position), down kernel
 // forms split partials over (chunk of the list) x (2048-column block).
 // ---------------------------------------------------------------------------
-template <bool REGLU>
+// FP8: the rows are E4M3 codes (d bytes each, 8 codes per 8-byte load) and
+// a dot product is multiplied by its row's scale before the bias.
+template <bool REGLU, bool FP8>
 __global__ void __launch_bounds__(256) k_sparse_up(
-    const __half *__restrict__ W_up, const __half *__restrict__ W_gate,
-    const float *__restrict__ bias, const __half *__restrict__ x, int B, int d, int ffn,
-    const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p, int count_const,
+    const void *__restrict__ R_up, const void *__restrict__ R_gate, const float *__restrict__ sc_up,
+    const float *__restrict__ sc_gate, const float *__restrict__ bias, const __half *__restrict__ x, int B,
+    int d, int ffn, const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p, int count_const,
     float *__restrict__ a, unsigned int *status, int silu) {
   pidev::griddep_wait();
   pidev::griddep_launch();
@@ -231,27 +233,41 @@ __global__ void __launch_bounds__(256) k_sparse_up(
 #pragma unroll
       for (int t = 0; t < kBT; ++t) su[t] = sg[t] = 0.f;
       if (ok) {
-        const uint4 *ru = reinterpret_cast<const uint4 *>(W_up + (size_t)i * d);
-        const uint4 *rg = reinterpret_cast<const uint4 *>(W_gate + (size_t)(REGLU ? i : 0) * d);
+        const size_t rb = FP8 ? (size_t)d : (size_t)d * 2;     // bytes per row
+        const char *ru = static_cast<const char *>(R_up) + (size_t)i * rb;
+        const char *rg = static_cast<const char *>(R_gate) + (size_t)(REGLU ? i : 0) * rb;
 #pragma unroll 2
         for (int v = lane; v < nv; v += 32) {
-          const uint4 wu = pidev::ld_stream(ru + v);
-          uint4 wg = make_uint4(0, 0, 0, 0);
-          if (REGLU) wg = pidev::ld_stream(rg + v);
+          uint4 wu = make_uint4(0, 0, 0, 0), wg = make_uint4(0, 0, 0, 0);
+          uint2 qu = make_uint2(0, 0), qg = make_uint2(0, 0);
+          if (FP8) {
+            qu = pidev::ld_stream2(reinterpret_cast<const uint2 *>(ru) + v);
+            if (REGLU) qg = pidev::ld_stream2(reinterpret_cast<const uint2 *>(rg) + v);
+          } else {
+            wu = pidev::ld_stream(reinterpret_cast<const uint4 *>(ru) + v);
+            if (REGLU) wg = pidev::ld_stream(reinterpret_cast<const uint4 *>(rg) + v);
+          }
 #pragma unroll
           for (int t = 0; t < kBT; ++t) {
             if (t < nb) {
               const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(b0 + t) * d) + v);
-              su[t] = pidev::dot8(su[t], wu, xv);
-              if (REGLU) sg[t] = pidev::dot8(sg[t], wg, xv);
+              if (FP8) {
+                su[t] = pidev::dot8_e4m3(su[t], qu, xv);
+                if (REGLU) sg[t] = pidev::dot8_e4m3(sg[t], qg, xv);
+              } else {
+                su[t] = pidev::dot8(su[t], wu, xv);
+                if (REGLU) sg[t] = pidev::dot8(sg[t], wg, xv);
+              }
             }
           }
         }
       }
+      const float scu = (FP8 && ok) ? sc_up[i] : 1.f;
+      const float scg = (FP8 && REGLU && ok) ? sc_gate[i] : 1.f;
 #pragma unroll
       for (int t = 0; t < kBT; ++t) {
-        const float u = pidev::warp_sum(su[t]);
-        const float g = REGLU ? pidev::warp_sum(sg[t]) : 0.f;
+        const float u = pidev::warp_sum(su[t]) * scu;
+        const float g = REGLU ? pidev::warp_sum(sg[t]) * scg : 0.f;
         if (lane == 0 && t < nb) {
           float av = 0.f;
           if (ok) {
@@ -270,9 +286,10 @@ __global__ void __launch_bounds__(256) k_sparse_up(
   }
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(256) k_sparse_down(
-    const __half *__restrict__ W_dT, const float *__restrict__ a, int B, int d, int ffn,
-    const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p, int count_const,
+    const void *__restrict__ R_dT, const float *__restrict__ sc_dT, const float *__restrict__ a, int B, int d,
+    int ffn, const int32_t *__restrict__ idx, const int32_t *__restrict__ count_p, int count_const,
     float *__restrict__ partial, unsigned int *status) {
   pidev::griddep_wait();
   pidev::griddep_launch();
@@ -295,10 +312,20 @@ __global__ void __launch_bounds__(256) k_sparse_down(
       for (int k = k0; k < k1; ++k) {
         const int i = idx ? idx[k] : k;
         if (i < 0 || i >= ffn) continue;   // flagged by the up kernel
-        const uint4 w = pidev::ld_stream(reinterpret_cast<const uint4 *>(W_dT + (size_t)i * d) + v);
+        if (FP8) {
+          const uint2 q = pidev::ld_stream2(
+              reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(R_dT) + (size_t)i * d) + v);
+          const float sc = sc_dT[i];
 #pragma unroll
-        for (int t = 0; t < kBT; ++t)
-          if (t < nb) pidev::axpy8(acc[t], a[(size_t)(b0 + t) * ffn + k], w);
+          for (int t = 0; t < kBT; ++t)
+            if (t < nb) pidev::axpy8_e4m3(acc[t], a[(size_t)(b0 + t) * ffn + k] * sc, q);
+        } else {
+          const uint4 w = pidev::ld_stream(
+              reinterpret_cast<const uint4 *>(static_cast<const __half *>(R_dT) + (size_t)i * d) + v);
+#pragma unroll
+          for (int t = 0; t < kBT; ++t)
+            if (t < nb) pidev::axpy8(acc[t], a[(size_t)(b0 + t) * ffn + k], w);
+        }
       }
       for (int t = 0; t < nb; ++t) {
         float4 *dst = reinterpret_cast<float4 *>(partial + ((size_t)blockIdx.x * B + b0 + t) * d) + 2 * v;
@@ -403,13 +430,16 @@ cudaError_t run_reduce(const float *partial, int nsplit, int n, float *y, cudaSt
 cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                            const int32_t *count, int count_const, float *y, const WsLayout &w,
                            char *ws, cudaStream_t s) {
-  if (B > 2 && tc_supported(L, B)) return run_sparse_ffn_tc(L, x, B, idx, count, count_const, y, w, ws, s);
+  // E4M3 rows: the generic kernels at every batch size (the decode step has
+  // its own E4M3 path; the fused and tensor-core kernels take fp16 rows)
+  const bool q8 = L->row_format == PI_ROWS_FP8_E4M3;
+  if (B > 2 && !q8 && tc_supported(L, B)) return run_sparse_ffn_tc(L, x, B, idx, count, count_const, y, w, ws, s);
   float *partial = reinterpret_cast<float *>(ws + w.partial);
   const bool reglu = L->act != PI_ACT_RELU;      // gated: ReGLU or SwiGLU
   const int silu = L->act == PI_ACT_SWIGLU ? 1 : 0;
   cudaError_t e;
   int nsplit;
-  if (B <= 2) {
+  if (B <= 2 && !q8) {
     nsplit = fused_splits(L);
     e = record_hook(L->ev_before, s);
     if (e != cudaSuccess) return e;
@@ -426,16 +456,27 @@ cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int3
     const int grid_up = L->num_sms * 4;
     e = record_hook(L->ev_before, s);
     if (e != cudaSuccess) return e;
-    e = reglu ? launch_pdl(k_sparse_up<true>, dim3(grid_up), dim3(256), 0, s, L->W_up, L->W_gate,
-                           L->b, x, B, L->d, L->ffn, idx, count, count_const, a, L->status, silu)
-              : launch_pdl(k_sparse_up<false>, dim3(grid_up), dim3(256), 0, s, L->W_up,
-                           L->W_gate, L->b, x, B, L->d, L->ffn, idx, count, count_const, a,
-                           L->status, silu);
+    const void *ru = q8 ? (const void *)L->Q_up : (const void *)L->W_up;
+    const void *rg = q8 ? (const void *)L->Q_gate : (const void *)L->W_gate;
+    const void *rd = q8 ? (const void *)L->Q_dT : (const void *)L->W_dT;
+    const dim3 gu(grid_up), bu(256);
+    if (q8)
+      e = reglu ? launch_pdl(k_sparse_up<true, true>, gu, bu, 0, s, ru, rg, L->s_up, L->s_gate, L->b, x, B, L->d,
+                             L->ffn, idx, count, count_const, a, L->status, silu)
+                : launch_pdl(k_sparse_up<false, true>, gu, bu, 0, s, ru, rg, L->s_up, L->s_gate, L->b, x, B, L->d,
+                             L->ffn, idx, count, count_const, a, L->status, silu);
+    else
+      e = reglu ? launch_pdl(k_sparse_up<true, false>, gu, bu, 0, s, ru, rg, L->s_up, L->s_gate, L->b, x, B, L->d,
+                             L->ffn, idx, count, count_const, a, L->status, silu)
+                : launch_pdl(k_sparse_up<false, false>, gu, bu, 0, s, ru, rg, L->s_up, L->s_gate, L->b, x, B, L->d,
+                             L->ffn, idx, count, count_const, a, L->status, silu);
     if (e != cudaSuccess) return e;
     nsplit = down_splits(L, B);
-    e = launch_pdl(k_sparse_down, dim3(nsplit, down_colblocks(L)), dim3(256), 0, s, L->W_dT,
-                   (const float *)a, B, L->d, L->ffn, idx, count, count_const, partial,
-                   L->status);
+    const dim3 gd(nsplit, down_colblocks(L)), bd(256);
+    e = q8 ? launch_pdl(k_sparse_down<true>, gd, bd, 0, s, rd, (const float *)L->s_dT, (const float *)a, B, L->d,
+                        L->ffn, idx, count, count_const, partial, L->status)
+           : launch_pdl(k_sparse_down<false>, gd, bd, 0, s, rd, (const float *)L->s_dT, (const float *)a, B, L->d,
+                        L->ffn, idx, count, count_const, partial, L->status);
     if (e != cudaSuccess) return e;
     e = record_hook(L->ev_after, s);
   }

@@ -374,8 +374,6 @@ def main():
     T = args.tokens or cfg.tokens
     batches = [int(b) for b in str(args.batch).split(",")]
     rows = args.rows
-    if rows == "fp8" and max(batches) > 2:
-        raise SystemExit("--rows fp8 runs at batch 1 or 2 (the persistent decode step)")
     # the CPU baseline times the fp16 oracle; it belongs to the fp16 workload
     want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1 and 1 in batches and rows == "fp16"
     t_setup = time.perf_counter()

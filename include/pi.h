@@ -121,10 +121,12 @@ typedef struct {
  * copy finished on `stream`.  The caller may free its buffers afterwards.
  * With row_format PI_ROWS_FP8_E4M3 the permuted up / gate / down^T rows are
  * quantised on the device as described at pi_row_format and only the codes
- * and scales are kept (d + 4 bytes per row); such a layer runs in
- * pi_predict, pi_compact_active, and pi_layer_forward / pi_stack_forward for
- * batches of 1 or 2 tokens; the other entry points return
- * PI_ERR_UNSUPPORTED for it.
+ * and scales are kept (d + 4 bytes per row).  Such a layer runs in every
+ * entry point but pi_sparse_ffn_noalloc (PI_ERR_UNSUPPORTED): the decode step
+ * of pi_layer_forward / pi_stack_forward (1 or 2 tokens) reads the codes in
+ * its persistent kernel; pi_sparse_ffn, pi_ffn_dense_ref and the batches of
+ * 3 or more tokens read them in the generic CUDA-core kernels (the
+ * tensor-core path takes fp16 rows only).
  * Errors: PI_ERR_INVALID_ARG (NULL pointer, bad perm, unknown row_format),
  * PI_ERR_UNSUPPORTED (shape), PI_ERR_OOM, PI_ERR_CUDA. *out is NULL on
  * failure. */

@@ -1,6 +1,8 @@
 """FP8 (E4M3) row layers on the GPU against the float64 oracle: the stored
-codes and scales byte for byte, and the decode step (pi_layer_forward /
-pi_stack_forward at 1 and 2 tokens) against the FFN of the dequantised rows."""
+codes and scales byte for byte, and every entry point that reads the rows
+(the decode step of pi_layer_forward / pi_stack_forward at 1 and 2 tokens,
+pi_sparse_ffn, pi_ffn_dense_ref, batches of 3 or more tokens) against the
+FFN of the dequantised rows."""
 import numpy as np
 import pytest
 import torch
@@ -85,21 +87,56 @@ def test_stack_of_fp8_layers(pi):
         check_y(y[l].cpu().numpy(), oracle_y_for_valid_set(L8, x[l], S))
 
 
-def test_fp8_layers_reject_the_fp16_only_entry_points(pi):
+@pytest.mark.parametrize("act,d,ffn,r", SHAPES)
+@pytest.mark.parametrize("B", [1, 2, 3, 8])
+def test_sparse_and_dense_operators_on_fp8_rows(pi, act, d, ffn, r, B):
+    """pi_sparse_ffn over a given set and pi_ffn_dense_ref over every neuron
+    read the E4M3 codes (generic CUDA-core kernels) and match the FFN of the
+    dequantised rows; two runs agree bitwise."""
+    spec = LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1)
+    t = make_layer(spec, 25, 0)
+    layer = pi.Layer.from_dict(to_dev(t), rows="fp8")
+    L8 = Q.fp8_layer(stored_oracle(layer, t))
+    x = make_tokens(d, B, seed=40 + B)
+    S = np.sort(np.random.default_rng(B).choice(ffn, size=ffn // 7, replace=False)).astype(np.int64)
+    idx = torch.from_numpy(S.astype(np.int32)).cuda()
+    count = torch.tensor([S.size], dtype=torch.int32, device="cuda")
+    y = layer.sparse_ffn(x.cuda(), idx, count)
+    y2 = layer.sparse_ffn(x.cuda(), idx, count)
+    yd = layer.dense_ref(x.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    rows = list(range(B)) if B <= 3 else [0, B - 1]
+    check_y(y.cpu().numpy()[rows], O.sparse_ffn(L8, x[rows], S))
+    check_y(yd.cpu().numpy()[rows], O.dense_ffn(L8, x[rows]))
+    assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("B", [3, 8, 32])
+def test_batched_forward_on_fp8_rows(pi, B):
+    """Batches of 3 or more tokens: the batched predictor (fp16 predictor
+    weights, so the same sets as the fp16 layer) and the E4M3 rows through
+    the generic kernels."""
+    act, d, ffn, r = "reglu", 2048, 3000, 128
+    spec = LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1)
+    t = make_layer(spec, 26, 0)
+    layer = pi.Layer.from_dict(to_dev(t), rows="fp8")
+    L8 = Q.fp8_layer(stored_oracle(layer, t))
+    x = make_tokens(d, B, seed=50 + B)
+    y, idx, count = layer.forward(x.cuda())
+    torch.cuda.synchronize()
+    S = idx[:int(count.item())].cpu().numpy().astype(np.int64)
+    h = O.predictor_hidden(L8, x)
+    check_union_set(S, O.predictor_logits(L8, h), O.logit_error_bound(L8, x, h, split=True))
+    rows = [0, B // 2, B - 1]
+    check_y(y.cpu().numpy()[rows], oracle_y_for_valid_set(L8, x[rows], S))
+    assert layer.device_status() == 0
+
+
+def test_fp8_row_access(pi):
     spec = LayerSpec(d=256, ffn=512, rank=16, mean_f=0.2)
     t = to_dev(make_layer(spec, 24, 0))
     layer = pi.Layer.from_dict(t, rows="fp8")
-    x = make_tokens(256, 3, seed=2).cuda()
-    y = torch.empty(3, 256, dtype=torch.float32, device="cuda")
-    idx = torch.arange(512, dtype=torch.int32, device="cuda")
-    count = torch.tensor([512], dtype=torch.int32, device="cuda")
-    for call in (lambda: layer.sparse_ffn(x[:1], idx, count, y[:1]),
-                 lambda: layer.dense_ref(x[:1], y[:1]),
-                 lambda: layer.forward(x, idx=torch.empty(512, dtype=torch.int32, device="cuda"),
-                                       count=torch.empty(1, dtype=torch.int32, device="cuda"), y=y)):
-        with pytest.raises(pi.PiError) as e:
-            call()
-        assert e.value.status == 2                  # PI_ERR_UNSUPPORTED
     with pytest.raises(pi.PiError):
         layer.rows_fp8(1)                           # no gate rows in a ReLU layer
     fp16 = pi.Layer.from_dict(t)

@@ -71,6 +71,11 @@ def test_noalloc_rejects_what_does_not_fit(pi):
     y = torch.empty(3, d, dtype=torch.float32, device="cuda")
     assert _noalloc(pi, layer, x, idx, count, y) == 2          # batch of 3
     assert b"1 or 2 tokens" in pi.lib.pi_last_error()
+    small = make_layer(LayerSpec(d=256, ffn=512, rank=16, mean_f=0.2), 24)
+    q8 = pi.Layer.from_dict(to_dev(small), rows="fp8")          # E4M3 rows: fp16 only here
+    xs = make_tokens(256, 1, seed=2).cuda()
+    assert _noalloc(pi, q8, xs, idx, count, y[:1, :256].contiguous()) == 2
+    assert b"fp16 rows" in pi.lib.pi_last_error()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     need = 4 * sms * 2 * d                                      # one split per SM above d = 2048
     st = _noalloc(pi, layer, x[:2], idx, count, y[:2])
