@@ -430,10 +430,11 @@ cudaError_t run_reduce(const float *partial, int nsplit, int n, float *y, cudaSt
 cudaError_t run_sparse_ffn(const pi_layer *L, const __half *x, int B, const int32_t *idx,
                            const int32_t *count, int count_const, float *y, const WsLayout &w,
                            char *ws, cudaStream_t s) {
-  // E4M3 rows: the generic kernels at every batch size (the decode step has
-  // its own E4M3 path; the fused and tensor-core kernels take fp16 rows)
+  // E4M3 rows: the tensor-core path converts the codes in shared memory; the
+  // generic kernels take them below 3 tokens (the decode step has its own
+  // E4M3 path) and for shapes off the tensor cores
   const bool q8 = L->row_format == PI_ROWS_FP8_E4M3;
-  if (B > 2 && !q8 && tc_supported(L, B)) return run_sparse_ffn_tc(L, x, B, idx, count, count_const, y, w, ws, s);
+  if (B > 2 && tc_supported(L, B)) return run_sparse_ffn_tc(L, x, B, idx, count, count_const, y, w, ws, s);
   float *partial = reinterpret_cast<float *>(ws + w.partial);
   const bool reglu = L->act != PI_ACT_RELU;      // gated: ReGLU or SwiGLU
   const int silu = L->act == PI_ACT_SWIGLU ? 1 : 0;

@@ -184,10 +184,17 @@ __device__ __forceinline__ int tile_row(const int32_t *idx, int k, int count, in
 // Epilogue of one tile row (the calling thread's row q, W row i, output
 // column kq).  fetch8(c, v) yields D columns c .. c+7 of the row; for kAct
 // and kHidden only token columns [c_begin, c_end) are produced.
+// Row scales of E4M3 layers for the kAct epilogue (all null for fp16 rows):
+// g / u multiply the gated / up dot products, d (the row's W_down^T scale)
+// multiplies the activation, which is how the down product's rows get it.
+struct RowScales {
+  const float *g = nullptr, *u = nullptr, *d = nullptr;
+};
+
 template <int MODE, bool REGLU, typename F>
 __device__ __forceinline__ bool row_epilogue(F fetch8, int c_begin, int c_end, int i, int kq, float bi, int B,
                                              int Bp, int Nmma, __half *abuf, int abuf_ld, uint8_t *mask_out,
-                                             bool silu) {
+                                             bool silu, const RowScales &sc) {
   // silu: the gate of a gated (kAct, REGLU) row is SiLU (SwiGLU) instead of ReLU
   if (MODE == kLogits) {                // kLogits: token columns [c_begin, c_end); returns l > 0 for one of them
     bool on = false;
@@ -202,6 +209,12 @@ __device__ __forceinline__ bool row_epilogue(F fetch8, int c_begin, int c_end, i
     if (i >= 0 && mask_out) mask_out[i] = on ? 1 : 0;
     return on;
   } else {
+    float sgi = 1.f, sui = 1.f, sdi = 1.f;
+    if (i >= 0) {
+      if (sc.g) sgi = sc.g[i];
+      if (sc.u) sui = sc.u[i];
+      if (sc.d) sdi = sc.d[i];
+    }
     for (int c0 = c_begin; c0 < c_end; c0 += 8) {
       float g8[8], u8[8];
       fetch8(c0, g8);
@@ -211,8 +224,9 @@ __device__ __forceinline__ bool row_epilogue(F fetch8, int c_begin, int c_end, i
         const int b = c0 + j;
         float a = 0.f;
         if (i >= 0 && b < B) {
-          const float z = g8[j] + bi;
-          a = REGLU ? pidev::gate_act(z, silu) * u8[j] : (z > 0.f ? z : 0.f);
+          const float z = g8[j] * sgi + bi;
+          a = REGLU ? pidev::gate_act(z, silu) * (u8[j] * sui) : (z > 0.f ? z : 0.f);
+          a *= sdi;
         }
         const __half hi = __float2half_rn(a);
         const __half lo = __float2half_rn(a - __half2float(hi));
@@ -382,7 +396,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
       const int i = rows_s[q];
       const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
       const bool on = row_epilogue<MODE, REGLU>([&](int c, float *v) { tmem_ld8(trow + (uint32_t)c, v); }, 0, Bp,
-                                                i, k0 + q, bi, B, Bp, Nmma, abuf, abuf_ld, mask_out, silu != 0);
+                                                i, k0 + q, bi, B, Bp, Nmma, abuf, abuf_ld, mask_out, silu != 0,
+                                                RowScales{});
       if (MODE == kLogits) {            // active rows of the tile, for the ordered compaction
         const int n_on = __syncthreads_count(on && i >= 0);
         if (tid == 0) tile_cnt[tile] = n_on;
@@ -408,6 +423,213 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
 }
 
+// ---------------------------------------------------------------------------
+// E4M3 rows on the tensor cores.  The MMA takes fp16 operands, so each stage
+// goes through shared memory twice: the codes of a stage are copied with
+// 16-byte cp.async into a ring of kRaw raw stages (each thread copies, and
+// later reads, its own stretch: 16 bytes of padding per stretch keep the
+// reads of a quarter-warp on distinct banks), and once a thread's copies of
+// the stage have landed (cp.async.wait_group) it converts them to fp16 in the
+// 128-byte-swizzled operand buffer (E4M3 values are exact in fp16) and
+// arrives on the stage's barrier.  One operand buffer: a stage is converted
+// when the MMAs of the one before it completed, while kRaw stages of codes
+// are in flight.  The row scales enter the up epilogue (the W_down^T row
+// scale multiplies the activation).
+constexpr int kRaw = 3;
+
+__device__ __forceinline__ void e4m3x16_to_half(const uint4 &q, uint4 &h0, uint4 &h1) {
+  const __nv_fp8x2_storage_t *p = reinterpret_cast<const __nv_fp8x2_storage_t *>(&q);
+  uint32_t o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(p[e], __NV_E4M3);
+    o[e] = (uint32_t)r.x | ((uint32_t)r.y << 16);
+  }
+  h0 = make_uint4(o[0], o[1], o[2], o[3]);
+  h1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__device__ __forceinline__ void mb_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
+// Up rows (kAct) of an E4M3 layer: Qg the gated rows (the up rows for ReLU),
+// Qu the up rows of a gated layer.  Thread t owns row t of the tile.
+template <bool REGLU>
+__global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict__ Qg, const uint8_t *__restrict__ Qu,
+                                                       const __grid_constant__ CUtensorMap tm_x,
+                                                       const int32_t *__restrict__ idx,
+                                                       const int32_t *__restrict__ count_p, int count_const,
+                                                       const float *__restrict__ bias, int d, int ffn, int B, int Bp,
+                                                       int kw, __half *__restrict__ abuf, int abuf_ld,
+                                                       float *__restrict__ piece, unsigned int *status, int silu,
+                                                       RowScales sc) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  constexpr int NA = REGLU ? 2 : 1;
+  const int Nmma = Bp;
+  const int ncolD = NA * Nmma;
+  const uint32_t slabA = kTile * 128;
+  const uint32_t slabX = (uint32_t)Nmma * 128;
+  const uint32_t subX = (slabX + 1023) & ~1023u;
+  const uint32_t a_bytes = (uint32_t)kw * (NA * slabA + subX);   // the operand stage
+  const uint32_t rrow = (uint32_t)kw * kSlab + 16;                // a thread's raw stretch per matrix
+  const uint32_t raw_bytes = NA * kTile * rrow;                   // one raw stage
+  unsigned char *opA = sm;
+  unsigned char *raw = sm + a_bytes;
+  __shared__ __align__(8) unsigned long long full_s, empty_s, done_s;
+  __shared__ int rows_s[kTile];
+  __shared__ uint32_t taddr_s;
+  __shared__ int fail_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ncols = tmem_cols_for(ncolD);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    mb_init(su32(&full_s), 129);      // 128 converting threads + the TMA expect_tx arrival
+    mb_init(su32(&empty_s), 1);
+    mb_init(su32(&done_s), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fail_s = 0;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = taddr_s;
+  pidev::griddep_wait();
+  pidev::griddep_launch();
+
+  int count = count_p ? *count_p : count_const;
+  if (count < 0 || count > ffn) {
+    if (tid == 0) atomicOr(status, PI_STATUS_BAD_COUNT);
+    count = count < 0 ? 0 : ffn;
+  }
+  const int ntiles = (count + kTile - 1) / kTile;
+  const int KT = d / (kSlab * kw);                      // stages per tile
+  const long long I = (long long)ntiles * KT;
+  const int G = active_ctas(gridDim.x, ntiles), cta = blockIdx.x;
+  const long long rs = cta < G ? range_start(cta, I, G) : 0, re = cta < G ? range_start(cta + 1, I, G) : 0;
+  const uint32_t idesc = idesc_f16(Nmma, kTile, false);
+  const uint32_t my_raw = su32(raw) + (uint32_t)tid * rrow;
+  const uint32_t full = su32(&full_s), empty = su32(&empty_s);
+  uint32_t gst = 0;            // operand stages used so far
+  uint32_t done_phase = 0;
+
+  for (long long s0 = rs; s0 < re;) {
+    const int tile = (int)(s0 / KT);
+    const int kb = (int)(s0 % KT);
+    const int n = (int)min((long long)(KT - kb), re - s0);   // stages of this piece
+    const bool whole = (n == KT);
+    const int slot = 2 * cta + (s0 == rs ? 0 : 1);
+    s0 += n;
+    const int k0 = tile * kTile;
+    rows_s[tid] = tile_row(idx, k0 + tid, count, ffn, status);
+    __syncthreads();
+    const int rid = rows_s[tid] >= 0 ? rows_s[tid] : 0;   // invalid / padding rows read row 0 (activation 0)
+    const uint8_t *gsrc = Qg + (size_t)rid * d;
+    const uint8_t *usrc = REGLU ? Qu + (size_t)rid * d : nullptr;
+    auto issue_raw = [&](int kt, int rslot) {
+      const uint32_t dst = my_raw + (uint32_t)rslot * raw_bytes;
+      const int off = kt * kw * kSlab;                  // byte (= code) offset in the row
+      for (int c = 0; c < 4 * kw; ++c) {
+        cp16(dst + c * 16, gsrc + off + c * 16);
+        if (REGLU) cp16(dst + kTile * rrow + c * 16, usrc + off + c * 16);
+      }
+    };
+    for (int p = 0; p < kRaw; ++p) {
+      if (p < n) issue_raw(kb + p, p);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int it = 0; it < n; ++it) {
+      if (fail_s) break;
+      const uint32_t g = gst + (uint32_t)it;
+      if (g >= 1 && !mb_wait(empty, (g - 1) & 1)) fail_s = 1;   // the previous stage's MMAs are done
+      if (tid == 0) {
+        mb_expect(full, kw * slabX);
+        for (int j = 0; j < kw; ++j)
+          tma_tile2d(su32(opA + NA * kw * slabA + j * subX), &tm_x, ((kb + it) * kw + j) * kSlab, 0, full);
+      }
+      asm volatile("cp.async.wait_group %0;" ::"n"(kRaw - 1) : "memory");
+      {
+        const unsigned char *src = raw + (size_t)(it % kRaw) * raw_bytes + (size_t)tid * rrow;
+#pragma unroll
+        for (int m = 0; m < NA; ++m)
+          for (int j = 0; j < kw; ++j) {
+            unsigned char *dstA = opA + (size_t)(m * kw + j) * slabA;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint4 q = *reinterpret_cast<const uint4 *>(src + m * kTile * rrow + j * kSlab + c * 16);
+              uint4 h0, h1;
+              e4m3x16_to_half(q, h0, h1);
+              *reinterpret_cast<uint4 *>(dstA + sw128(tid, 2 * c)) = h0;
+              *reinterpret_cast<uint4 *>(dstA + sw128(tid, 2 * c + 1)) = h1;
+            }
+          }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mb_arrive(full);
+      if (it + kRaw < n) issue_raw(kb + it + kRaw, it % kRaw);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (tid == 0) {
+        if (!mb_wait(full, g & 1)) {
+          fail_s = 1;
+        } else {
+          asm volatile("tcgen05.fence::after_thread_sync;");
+          for (int j = 0; j < kw; ++j) {
+            const uint32_t xa = su32(opA + NA * kw * slabA + j * subX);
+            const uint32_t aa = su32(opA + j * slabA);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = sdesc(xa + kk * 32, 16, 1024);
+              const uint32_t acc = (it | j | kk) ? 1u : 0u;
+              mma_f16(tmem, sdesc(aa + kk * 32, 16, 1024), bd, idesc, acc);
+              if (REGLU) mma_f16(tmem + (uint32_t)Nmma, sdesc(aa + kw * slabA + kk * 32, 16, 1024), bd, idesc, acc);
+            }
+          }
+          mma_commit(empty);
+        }
+      }
+    }
+    gst += (uint32_t)n;
+    if (tid == 0) mma_commit(su32(&done_s));
+    __syncthreads();
+    if (fail_s) break;
+    if (!mb_wait(su32(&done_s), done_phase)) { fail_s = 1; break; }
+    done_phase ^= 1u;
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const int q = warp * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    if (whole) {
+      const int i = rows_s[q];
+      const float bi = (i >= 0 && bias) ? bias[i] : 0.f;
+      row_epilogue<kAct, REGLU>([&](int c, float *v) { tmem_ld8(trow + (uint32_t)c, v); }, 0, Bp, i, k0 + q, bi, B,
+                                Bp, Nmma, abuf, abuf_ld, nullptr, silu != 0, sc);
+    } else {
+      float *dst = piece + (size_t)slot * ncolD * kTile + q;
+      for (int c0 = 0; c0 < ncolD; c0 += 8) {
+        float v[8];
+        tmem_ld8(trow + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[(size_t)(c0 + j) * kTile] = v[j];
+      }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+  }
+  // every copy this CTA issued lands before it leaves (the waits are bounded)
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (fail_s && tid == 0) {
+    atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
+    mb_wait(full, 0), mb_wait(full, 1);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
+}
+
 // Tiles that k_tc_rows split between CTAs: block c finishes the tile whose
 // last stage lies in CTA c's range when that tile started in an earlier CTA's
 // range.  It adds the tile's pieces in CTA order and applies the epilogue;
@@ -419,7 +641,7 @@ __global__ void __launch_bounds__(1024) k_tc_fixup(const float *__restrict__ pie
                                                    const float *__restrict__ bias, int ffn, int B, int Bp, int KT,
                                                    int grid, __half *__restrict__ abuf, int abuf_ld,
                                                    uint8_t *__restrict__ mask_out, int32_t *__restrict__ tile_cnt,
-                                                   unsigned int *status, int silu) {
+                                                   unsigned int *status, int silu, RowScales sc) {
   pidev::griddep_wait();
   pidev::griddep_launch();
   constexpr int NA = REGLU ? 2 : 1;
@@ -482,7 +704,7 @@ __global__ void __launch_bounds__(1024) k_tc_fixup(const float *__restrict__ pie
   bool on = false;
   for (int c0 = 8 * grp; c0 < Bp; c0 += 8 * ngrp)
     on |= row_epilogue<MODE, REGLU>(fetch8, c0, c0 + 8, i, tile * kTile + q, bi, B, Bp, Nmma, abuf, abuf_ld,
-                                    nullptr, silu != 0);
+                                    nullptr, silu != 0, sc);
   if (MODE == kLogits) {
     on_s[grp][q] = on ? 1 : 0;
     __syncthreads();
@@ -692,6 +914,163 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
 }
 
+// W_down^T rows of an E4M3 layer (the row scales are in the activations):
+// the units, pieces and MMAs of k_tc_down; thread t copies and converts half
+// of row t / 2 of the slab's codes for the column tile (cw * 64 codes).
+__global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict__ Qd,
+                                                       const __grid_constant__ CUtensorMap tm_a,
+                                                       const int32_t *__restrict__ idx,
+                                                       const int32_t *__restrict__ count_p, int count_const, int d,
+                                                       int ffn, int B, int Bp, int cw, float *__restrict__ piece,
+                                                       unsigned int *status) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+  const int N2 = 2 * Bp;
+  const uint32_t half_bytes = kSlab * 128;                // 64 rows x 64 columns
+  const uint32_t tileW = 2 * half_bytes;                  // 128 columns
+  const uint32_t slabW = (uint32_t)cw * tileW;
+  const uint32_t slabA = (uint32_t)N2 * 128;
+  const uint32_t a_bytes = slabW + ((slabA + 1023) & ~1023u);
+  const uint32_t rrow = (uint32_t)cw * 64 + 16;           // a thread's raw stretch (cw * 64 codes + padding)
+  const uint32_t raw_bytes = kTile * rrow;
+  const int CW = cw * kTile;                              // outputs per column tile
+  unsigned char *opA = sm;
+  unsigned char *raw = sm + a_bytes;
+  __shared__ __align__(8) unsigned long long full_s, empty_s, done_s;
+  __shared__ uint32_t taddr_s;
+  __shared__ int fail_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ncols = tmem_cols_for(cw * N2);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&taddr_s)), "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    mb_init(su32(&full_s), 129);
+    mb_init(su32(&empty_s), 1);
+    mb_init(su32(&done_s), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fail_s = 0;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = taddr_s;
+  pidev::griddep_wait();
+  pidev::griddep_launch();
+
+  int count = count_p ? *count_p : count_const;
+  if (count < 0 || count > ffn) count = count < 0 ? 0 : ffn;     // flagged by the up kernel
+  const int KS = (count + kSlab - 1) / kSlab;
+  const int ctiles = (d + CW - 1) / CW;
+  const long long I = (long long)ctiles * KS;
+  const int G = active_ctas(gridDim.x, ctiles), cta = blockIdx.x;
+  const long long rs = cta < G ? range_start(cta, I, G) : 0, re = cta < G ? range_start(cta + 1, I, G) : 0;
+  const uint32_t idesc = idesc_f16(N2, kTile, true);
+  const int q = tid >> 1, hb = tid & 1;                   // row of the slab, half of its codes
+  const uint32_t my_raw = su32(raw) + (uint32_t)tid * rrow;
+  const uint32_t full = su32(&full_s), empty = su32(&empty_s);
+  uint32_t gst = 0, done_phase = 0;
+
+  for (long long s0 = rs; s0 < re;) {
+    const int tile = (int)(s0 / KS);
+    const int kb = (int)(s0 % KS);
+    const int n = (int)min((long long)(KS - kb), re - s0);   // slabs of this piece
+    const int slot = 2 * cta + (s0 == rs ? 0 : 1);
+    s0 += n;
+    const int j0 = tile * CW;
+    auto issue_raw = [&](int slab, int rslot) {
+      const int k = slab * kSlab + q;
+      int rid = k < count ? (idx ? idx[k] : k) : 0;
+      if (rid < 0 || rid >= ffn) rid = 0;                   // padding / invalid: row 0 times a zero activation
+      const uint32_t dst = my_raw + (uint32_t)rslot * raw_bytes;
+      const int col0 = j0 + hb * cw * 64;
+      for (int c = 0; c < 4 * cw; ++c) {
+        const int col = col0 + 16 * c;
+        cp16(dst + c * 16, Qd + (size_t)rid * d + (col < d ? col : 0));   // a column past d: output dropped
+      }
+    };
+    for (int p = 0; p < kRaw; ++p) {
+      if (p < n) issue_raw(kb + p, p);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int it = 0; it < n; ++it) {
+      if (fail_s) break;
+      const uint32_t g = gst + (uint32_t)it;
+      if (g >= 1 && !mb_wait(empty, (g - 1) & 1)) fail_s = 1;
+      if (tid == 0) {
+        mb_expect(full, slabA);
+        tma_tile2d(su32(opA + slabW), &tm_a, (kb + it) * kSlab, 0, full);
+      }
+      asm volatile("cp.async.wait_group %0;" ::"n"(kRaw - 1) : "memory");
+      {
+        const unsigned char *src = raw + (size_t)(it % kRaw) * raw_bytes + (size_t)tid * rrow;
+        for (int c = 0; c < 4 * cw; ++c) {
+          const uint4 qv = *reinterpret_cast<const uint4 *>(src + c * 16);
+          uint4 h[2];
+          e4m3x16_to_half(qv, h[0], h[1]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int colr = hb * cw * 64 + 16 * c + 8 * e;   // column within the unit
+            const int ct = colr >> 7, hh = (colr >> 6) & 1, cch = (colr >> 3) & 7;
+            *reinterpret_cast<uint4 *>(opA + ct * tileW + hh * half_bytes + sw128(q, cch)) = h[e];
+          }
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mb_arrive(full);
+      if (it + kRaw < n) issue_raw(kb + it + kRaw, it % kRaw);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (tid == 0) {
+        if (!mb_wait(full, g & 1)) {
+          fail_s = 1;
+        } else {
+          asm volatile("tcgen05.fence::after_thread_sync;");
+          for (int c = 0; c < cw; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc(su32(opA) + c * tileW + kk * 16 * 128, half_bytes, 1024);
+              const uint64_t bd = sdesc(su32(opA + slabW) + kk * 32, 16, 1024);
+              mma_f16(tmem + (uint32_t)(c * N2), ad, bd, idesc, (it | kk) ? 1u : 0u);
+            }
+          mma_commit(empty);
+        }
+      }
+    }
+    gst += (uint32_t)n;
+    if (tid == 0) mma_commit(su32(&done_s));
+    __syncthreads();
+    if (fail_s) break;
+    if (!mb_wait(su32(&done_s), done_phase)) { fail_s = 1; break; }
+    done_phase ^= 1u;
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    for (int c = 0; c < cw; ++c) {
+      const int jl = c * kTile + warp * 32 + lane;           // TMEM lane = output column
+      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * N2);
+      float *dst = piece + (size_t)slot * B * CW + jl;
+      for (int c0 = 0; c0 < Bp; c0 += 8) {
+        float hi[8], lo[8];
+        tmem_ld8(trow + (uint32_t)c0, hi);
+        tmem_ld8(trow + (uint32_t)(Bp + c0), lo);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (c0 + e < B) dst[(size_t)(c0 + e) * CW] = hi[e] + lo[e];
+      }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (fail_s && tid == 0) {
+    atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
+    mb_wait(full, 0), mb_wait(full, 1);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols));
+}
+
 // y[b, j] = the pieces of j's column tile added in CTA order (0 for an empty
 // list).  Block (tile, b), one thread per column of the tile (up to 512):
 // thread 0 lists the tile's pieces once for the block.
@@ -802,7 +1181,43 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
   if (e != cudaSuccess) return e;
   const int groups = std::min(Bp / 8, 8);       // 128 threads per group of token columns
   return pi::launch_pdl(k_tc_fixup<MODE, REGLU>, dim3(G), dim3(kTile * groups), 0, s, piece, idx, count, count_const,
-                        bias, nrows, B, Bp, slabs / kw, G, out, out_ld, mask, tile_cnt, L->status, silu);
+                        bias, nrows, B, Bp, slabs / kw, G, out, out_ld, mask, tile_cnt, L->status, silu, RowScales{});
+}
+
+// The E4M3 up kernel and its fix-up: the widest stage (kw slabs) whose
+// operand buffer and kRaw raw stages fit in shared memory.
+template <bool REGLU>
+cudaError_t launch_rows_q8(const pi_layer *L, const CUtensorMap &tm_x, const int32_t *idx, const int32_t *count,
+                           int count_const, int B, int Bp, __half *out, int out_ld, float *piece, cudaStream_t s,
+                           int silu) {
+  constexpr int NA = REGLU ? 2 : 1;
+  const size_t subX = ((size_t)Bp * 128 + 1023) & ~(size_t)1023;
+  const int slabs = L->d / kSlab;
+  int kw = 4;
+  size_t smem = 0;
+  for (; kw >= 1; kw >>= 1) {
+    if (slabs % kw != 0) continue;
+    smem = 1024 + (size_t)kw * (NA * (size_t)kTile * 128 + subX) + kRaw * (size_t)NA * kTile * (kw * kSlab + 16);
+    if (smem <= kTcSmemBudget) break;
+  }
+  if (kw < 1) return cudaErrorInvalidValue;
+  RowScales sc;
+  sc.g = REGLU ? L->s_gate : L->s_up;
+  sc.u = REGLU ? L->s_up : nullptr;
+  sc.d = L->s_dT;
+  const uint8_t *Qg = REGLU ? L->Q_gate : L->Q_up;
+  const uint8_t *Qu = REGLU ? L->Q_up : nullptr;
+  const int G = L->num_sms;
+  auto kern = k_tc_rows_q8<REGLU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = pi::launch_pdl(kern, dim3(G), dim3(128), smem, s, Qg, Qu, tm_x, idx, count, count_const, (const float *)L->b,
+                     L->d, L->ffn, B, Bp, kw, out, out_ld, piece, L->status, silu, sc);
+  if (e != cudaSuccess) return e;
+  const int groups = std::min(Bp / 8, 8);
+  return pi::launch_pdl(k_tc_fixup<kAct, REGLU>, dim3(G), dim3(kTile * groups), 0, s, piece, idx, count, count_const,
+                        (const float *)L->b, L->ffn, B, Bp, slabs / kw, G, out, out_ld, (uint8_t *)nullptr,
+                        (int32_t *)nullptr, L->status, silu, sc);
 }
 
 }  // namespace
@@ -865,26 +1280,46 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
       !encode_2d(&tm_a, abuf, ffn_pad, 2 * Bp, (uint64_t)ffn_pad * 2, kSlab, 2 * Bp))
     return cudaErrorInvalidValue;
 
+  const bool q8 = L->row_format == PI_ROWS_FP8_E4M3;
   cudaError_t e = record_hook(L->ev_before, s);
   if (e != cudaSuccess) return e;
-  e = reglu ? launch_rows<kAct, true>(L, L->W_gate, L->W_up, tm_x, idx, count, count_const, L->b, L->d, L->d, L->ffn, B,
-                                      Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s, silu)
-            : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->d, L->ffn, B,
-                                       Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s);
+  if (q8)
+    e = reglu ? launch_rows_q8<true>(L, tm_x, idx, count, count_const, B, Bp, abuf, ffn_pad, piece, s, silu)
+              : launch_rows_q8<false>(L, tm_x, idx, count, count_const, B, Bp, abuf, ffn_pad, piece, s, silu);
+  else
+    e = reglu ? launch_rows<kAct, true>(L, L->W_gate, L->W_up, tm_x, idx, count, count_const, L->b, L->d, L->d, L->ffn,
+                                        B, Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s, silu)
+              : launch_rows<kAct, false>(L, L->W_up, nullptr, tm_x, idx, count, count_const, L->b, L->d, L->d, L->ffn,
+                                         B, Bp, abuf, ffn_pad, nullptr, piece, nullptr, false, s);
   if (e != cudaSuccess) return e;
 
   // down: stages of cw x 16 KB gathered W_down^T + the [a_hi; a_lo] slab
+  // (E4M3 rows: one such operand stage and kRaw raw stages of cw x 8 KB)
   int cw = kDownCwMax;
   while (cw > 1 && (L->d % (cw * kTile) != 0 || cw * 2 * Bp > 512)) cw >>= 1;
-  const size_t dn_stage = cw * 2 * (size_t)kSlab * 128 + (((size_t)2 * Bp * 128 + 1023) & ~(size_t)1023);
-  int dn_ns = (int)((kTcSmemBudget - 1024) / dn_stage);
-  if (dn_ns > 8) dn_ns = 8;
-  if (dn_ns < 2) return cudaErrorInvalidValue;
-  const size_t dn_smem = 1024 + dn_ns * dn_stage;
-  e = cudaFuncSetAttribute(k_tc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(k_tc_down, dim3(L->num_sms), dim3(128), dn_smem, s, L->W_dT, tm_a, idx, count, count_const, L->d,
-                 L->ffn, B, Bp, dn_ns, cw, piece, L->status);
+  const size_t act_slab = ((size_t)2 * Bp * 128 + 1023) & ~(size_t)1023;
+  if (q8) {
+    size_t dn_smem = 0;
+    for (;; cw >>= 1) {
+      dn_smem = 1024 + cw * 2 * (size_t)kSlab * 128 + act_slab + kRaw * (size_t)kTile * (cw * 64 + 16);
+      if (dn_smem <= kTcSmemBudget || cw == 1) break;
+    }
+    if (dn_smem > kTcSmemBudget) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(k_tc_down_q8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_tc_down_q8, dim3(L->num_sms), dim3(128), dn_smem, s, (const uint8_t *)L->Q_dT, tm_a, idx, count,
+                   count_const, L->d, L->ffn, B, Bp, cw, piece, L->status);
+  } else {
+    const size_t dn_stage = cw * 2 * (size_t)kSlab * 128 + act_slab;
+    int dn_ns = (int)((kTcSmemBudget - 1024) / dn_stage);
+    if (dn_ns > 8) dn_ns = 8;
+    if (dn_ns < 2) return cudaErrorInvalidValue;
+    const size_t dn_smem = 1024 + dn_ns * dn_stage;
+    e = cudaFuncSetAttribute(k_tc_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_tc_down, dim3(L->num_sms), dim3(128), dn_smem, s, L->W_dT, tm_a, idx, count, count_const, L->d,
+                   L->ffn, B, Bp, dn_ns, cw, piece, L->status);
+  }
   if (e != cudaSuccess) return e;
   e = record_hook(L->ev_after, s);
   if (e != cudaSuccess) return e;

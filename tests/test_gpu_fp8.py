@@ -88,11 +88,13 @@ def test_stack_of_fp8_layers(pi):
 
 
 @pytest.mark.parametrize("act,d,ffn,r", SHAPES)
-@pytest.mark.parametrize("B", [1, 2, 3, 8])
+@pytest.mark.parametrize("B", [1, 2, 3, 8, 32, 128])
 def test_sparse_and_dense_operators_on_fp8_rows(pi, act, d, ffn, r, B):
     """pi_sparse_ffn over a given set and pi_ffn_dense_ref over every neuron
-    read the E4M3 codes (generic CUDA-core kernels) and match the FFN of the
-    dequantised rows; two runs agree bitwise."""
+    read the E4M3 codes (1-2 tokens: generic CUDA-core kernels; 3 or more:
+    the tensor-core kernels, which convert the codes to fp16 in shared
+    memory) and match the FFN of the dequantised rows; two runs agree
+    bitwise."""
     spec = LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1)
     t = make_layer(spec, 25, 0)
     layer = pi.Layer.from_dict(to_dev(t), rows="fp8")
@@ -112,12 +114,13 @@ def test_sparse_and_dense_operators_on_fp8_rows(pi, act, d, ffn, r, B):
     assert layer.device_status() == 0
 
 
+@pytest.mark.parametrize("act,d,ffn,r", [("reglu", 2048, 3000, 128), ("relu", 4096, 20000, 256),
+                                         ("swiglu", 1024, 5000, 64)])
 @pytest.mark.parametrize("B", [3, 8, 32])
-def test_batched_forward_on_fp8_rows(pi, B):
+def test_batched_forward_on_fp8_rows(pi, act, d, ffn, r, B):
     """Batches of 3 or more tokens: the batched predictor (fp16 predictor
-    weights, so the same sets as the fp16 layer) and the E4M3 rows through
-    the generic kernels."""
-    act, d, ffn, r = "reglu", 2048, 3000, 128
+    weights, so the same sets as the fp16 layer) and the E4M3 rows on the
+    tensor cores (the W_down^T row scale carried by the activation)."""
     spec = LayerSpec(d=d, ffn=ffn, rank=r, act=act, mean_f=0.1)
     t = make_layer(spec, 26, 0)
     layer = pi.Layer.from_dict(to_dev(t), rows="fp8")
