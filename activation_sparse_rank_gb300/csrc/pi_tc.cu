@@ -454,8 +454,10 @@ __device__ __forceinline__ void mb_arrive(uint32_t mbar) {
 }
 
 // Up rows (kAct) of an E4M3 layer: Qg the gated rows (the up rows for ReLU),
-// Qu the up rows of a gated layer.  Thread t owns row t of the tile.
-template <bool REGLU>
+// Qu the up rows of a gated layer.  Thread t owns row t of the tile.  NOP
+// operand buffers: with two, the conversion of a stage overlaps the MMAs of
+// the one before it (and two raw stages are in flight instead of three).
+template <bool REGLU, int NOP>
 __global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict__ Qg, const uint8_t *__restrict__ Qu,
                                                        const __grid_constant__ CUtensorMap tm_x,
                                                        const int32_t *__restrict__ idx,
@@ -475,9 +477,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict
   const uint32_t a_bytes = (uint32_t)kw * (NA * slabA + subX);   // the operand stage
   const uint32_t rrow = (uint32_t)kw * kSlab + 16;                // a thread's raw stretch per matrix
   const uint32_t raw_bytes = NA * kTile * rrow;                   // one raw stage
-  unsigned char *opA = sm;
-  unsigned char *raw = sm + a_bytes;
-  __shared__ __align__(8) unsigned long long full_s, empty_s, done_s;
+  constexpr int KR = NOP == 2 ? 2 : kRaw;                         // raw stages in the ring
+  unsigned char *raw = sm + NOP * a_bytes;
+  __shared__ __align__(8) unsigned long long full_s[NOP], empty_s[NOP], done_s;
   __shared__ int rows_s[kTile];
   __shared__ uint32_t taddr_s;
   __shared__ int fail_s;
@@ -489,8 +491,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    mb_init(su32(&full_s), 129);      // 128 converting threads + the TMA expect_tx arrival
-    mb_init(su32(&empty_s), 1);
+    for (int b = 0; b < NOP; ++b) {
+      mb_init(su32(&full_s[b]), 129);   // 128 converting threads + the TMA expect_tx arrival
+      mb_init(su32(&empty_s[b]), 1);
+    }
     mb_init(su32(&done_s), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fail_s = 0;
@@ -514,8 +518,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict
   const long long rs = cta < G ? range_start(cta, I, G) : 0, re = cta < G ? range_start(cta + 1, I, G) : 0;
   const uint32_t idesc = idesc_f16(Nmma, kTile, false);
   const uint32_t my_raw = su32(raw) + (uint32_t)tid * rrow;
-  const uint32_t full = su32(&full_s), empty = su32(&empty_s);
-  uint32_t gst = 0;            // operand stages used so far
+  uint32_t gst = 0;            // operand stages used so far (buffer gst % NOP)
   uint32_t done_phase = 0;
 
   for (long long s0 = rs; s0 < re;) {
@@ -539,22 +542,26 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict
         if (REGLU) cp16(dst + kTile * rrow + c * 16, usrc + off + c * 16);
       }
     };
-    for (int p = 0; p < kRaw; ++p) {
+    for (int p = 0; p < KR; ++p) {
       if (p < n) issue_raw(kb + p, p);
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
     for (int it = 0; it < n; ++it) {
       if (fail_s) break;
       const uint32_t g = gst + (uint32_t)it;
-      if (g >= 1 && !mb_wait(empty, (g - 1) & 1)) fail_s = 1;   // the previous stage's MMAs are done
+      const int b = (int)(g % NOP);
+      unsigned char *opA = sm + (size_t)b * a_bytes;
+      const uint32_t full = su32(&full_s[b]), empty = su32(&empty_s[b]);
+      // this buffer's previous stage: its MMAs are done
+      if (g >= NOP && !mb_wait(empty, ((g / NOP) - 1) & 1)) fail_s = 1;
       if (tid == 0) {
         mb_expect(full, kw * slabX);
         for (int j = 0; j < kw; ++j)
           tma_tile2d(su32(opA + NA * kw * slabA + j * subX), &tm_x, ((kb + it) * kw + j) * kSlab, 0, full);
       }
-      asm volatile("cp.async.wait_group %0;" ::"n"(kRaw - 1) : "memory");
+      asm volatile("cp.async.wait_group %0;" ::"n"(KR - 1) : "memory");
       {
-        const unsigned char *src = raw + (size_t)(it % kRaw) * raw_bytes + (size_t)tid * rrow;
+        const unsigned char *src = raw + (size_t)(it % KR) * raw_bytes + (size_t)tid * rrow;
 #pragma unroll
         for (int m = 0; m < NA; ++m)
           for (int j = 0; j < kw; ++j) {
@@ -571,10 +578,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mb_arrive(full);
-      if (it + kRaw < n) issue_raw(kb + it + kRaw, it % kRaw);
+      if (it + KR < n) issue_raw(kb + it + KR, it % KR);
       asm volatile("cp.async.commit_group;" ::: "memory");
       if (tid == 0) {
-        if (!mb_wait(full, g & 1)) {
+        if (!mb_wait(full, (g / NOP) & 1)) {
           fail_s = 1;
         } else {
           asm volatile("tcgen05.fence::after_thread_sync;");
@@ -623,7 +630,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows_q8(const uint8_t *__restrict
   asm volatile("cp.async.wait_all;" ::: "memory");
   if (fail_s && tid == 0) {
     atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
-    mb_wait(full, 0), mb_wait(full, 1);
+    for (int b = 0; b < NOP; ++b) mb_wait(su32(&full_s[b]), 0), mb_wait(su32(&full_s[b]), 1);
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
@@ -916,7 +923,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_down(const __half *__restrict__ W
 
 // W_down^T rows of an E4M3 layer (the row scales are in the activations):
 // the units, pieces and MMAs of k_tc_down; thread t copies and converts half
-// of row t / 2 of the slab's codes for the column tile (cw * 64 codes).
+// of row t / 2 of the slab's codes for the column tile (cw * 64 codes); NOP
+// operand buffers as in k_tc_rows_q8.
+template <int NOP>
 __global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict__ Qd,
                                                        const __grid_constant__ CUtensorMap tm_a,
                                                        const int32_t *__restrict__ idx,
@@ -934,9 +943,9 @@ __global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict
   const uint32_t rrow = (uint32_t)cw * 64 + 16;           // a thread's raw stretch (cw * 64 codes + padding)
   const uint32_t raw_bytes = kTile * rrow;
   const int CW = cw * kTile;                              // outputs per column tile
-  unsigned char *opA = sm;
-  unsigned char *raw = sm + a_bytes;
-  __shared__ __align__(8) unsigned long long full_s, empty_s, done_s;
+  constexpr int KR = NOP == 2 ? 2 : kRaw;                 // raw stages in the ring
+  unsigned char *raw = sm + NOP * a_bytes;
+  __shared__ __align__(8) unsigned long long full_s[NOP], empty_s[NOP], done_s;
   __shared__ uint32_t taddr_s;
   __shared__ int fail_s;
 
@@ -947,8 +956,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    mb_init(su32(&full_s), 129);
-    mb_init(su32(&empty_s), 1);
+    for (int b = 0; b < NOP; ++b) {
+      mb_init(su32(&full_s[b]), 129);
+      mb_init(su32(&empty_s[b]), 1);
+    }
     mb_init(su32(&done_s), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fail_s = 0;
@@ -970,7 +981,6 @@ __global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict
   const uint32_t idesc = idesc_f16(N2, kTile, true);
   const int q = tid >> 1, hb = tid & 1;                   // row of the slab, half of its codes
   const uint32_t my_raw = su32(raw) + (uint32_t)tid * rrow;
-  const uint32_t full = su32(&full_s), empty = su32(&empty_s);
   uint32_t gst = 0, done_phase = 0;
 
   for (long long s0 = rs; s0 < re;) {
@@ -991,21 +1001,24 @@ __global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict
         cp16(dst + c * 16, Qd + (size_t)rid * d + (col < d ? col : 0));   // a column past d: output dropped
       }
     };
-    for (int p = 0; p < kRaw; ++p) {
+    for (int p = 0; p < KR; ++p) {
       if (p < n) issue_raw(kb + p, p);
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
     for (int it = 0; it < n; ++it) {
       if (fail_s) break;
       const uint32_t g = gst + (uint32_t)it;
-      if (g >= 1 && !mb_wait(empty, (g - 1) & 1)) fail_s = 1;
+      const int b = (int)(g % NOP);
+      unsigned char *opA = sm + (size_t)b * a_bytes;
+      const uint32_t full = su32(&full_s[b]), empty = su32(&empty_s[b]);
+      if (g >= NOP && !mb_wait(empty, ((g / NOP) - 1) & 1)) fail_s = 1;
       if (tid == 0) {
         mb_expect(full, slabA);
         tma_tile2d(su32(opA + slabW), &tm_a, (kb + it) * kSlab, 0, full);
       }
-      asm volatile("cp.async.wait_group %0;" ::"n"(kRaw - 1) : "memory");
+      asm volatile("cp.async.wait_group %0;" ::"n"(KR - 1) : "memory");
       {
-        const unsigned char *src = raw + (size_t)(it % kRaw) * raw_bytes + (size_t)tid * rrow;
+        const unsigned char *src = raw + (size_t)(it % KR) * raw_bytes + (size_t)tid * rrow;
         for (int c = 0; c < 4 * cw; ++c) {
           const uint4 qv = *reinterpret_cast<const uint4 *>(src + c * 16);
           uint4 h[2];
@@ -1020,10 +1033,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mb_arrive(full);
-      if (it + kRaw < n) issue_raw(kb + it + kRaw, it % kRaw);
+      if (it + KR < n) issue_raw(kb + it + KR, it % KR);
       asm volatile("cp.async.commit_group;" ::: "memory");
       if (tid == 0) {
-        if (!mb_wait(full, g & 1)) {
+        if (!mb_wait(full, (g / NOP) & 1)) {
           fail_s = 1;
         } else {
           asm volatile("tcgen05.fence::after_thread_sync;");
@@ -1064,7 +1077,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_down_q8(const uint8_t *__restrict
   asm volatile("cp.async.wait_all;" ::: "memory");
   if (fail_s && tid == 0) {
     atomicOr(status, PI_STATUS_BARRIER_TIMEOUT);
-    mb_wait(full, 0), mb_wait(full, 1);
+    for (int b = 0; b < NOP; ++b) mb_wait(su32(&full_s[b]), 0), mb_wait(su32(&full_s[b]), 1);
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
@@ -1184,8 +1197,11 @@ cudaError_t launch_rows(const pi_layer *L, const __half *Wg, const __half *Wu, c
                         bias, nrows, B, Bp, slabs / kw, G, out, out_ld, mask, tile_cnt, L->status, silu, RowScales{});
 }
 
-// The E4M3 up kernel and its fix-up: the widest stage (kw slabs) whose
-// operand buffer and kRaw raw stages fit in shared memory.
+// The E4M3 up kernel and its fix-up: the widest stage (kw slabs), with two
+// operand buffers and two raw stages if they fit in kQ8Smem2 bytes of shared
+// memory, else with one operand buffer and kRaw raw stages.
+constexpr size_t kQ8Smem2 = 225 * 1024;
+
 template <bool REGLU>
 cudaError_t launch_rows_q8(const pi_layer *L, const CUtensorMap &tm_x, const int32_t *idx, const int32_t *count,
                            int count_const, int B, int Bp, __half *out, int out_ld, float *piece, cudaStream_t s,
@@ -1193,14 +1209,22 @@ cudaError_t launch_rows_q8(const pi_layer *L, const CUtensorMap &tm_x, const int
   constexpr int NA = REGLU ? 2 : 1;
   const size_t subX = ((size_t)Bp * 128 + 1023) & ~(size_t)1023;
   const int slabs = L->d / kSlab;
-  int kw = 4;
+  int kw = 4, nop = 0;
   size_t smem = 0;
-  for (; kw >= 1; kw >>= 1) {
+  for (; kw >= 1 && nop == 0; kw >>= 1) {
     if (slabs % kw != 0) continue;
-    smem = 1024 + (size_t)kw * (NA * (size_t)kTile * 128 + subX) + kRaw * (size_t)NA * kTile * (kw * kSlab + 16);
-    if (smem <= kTcSmemBudget) break;
+    const size_t a = (size_t)kw * (NA * (size_t)kTile * 128 + subX);
+    const size_t raw = (size_t)NA * kTile * (kw * kSlab + 16);
+    if (1024 + 2 * a + 2 * raw <= kQ8Smem2) {
+      nop = 2;
+      smem = 1024 + 2 * a + 2 * raw;
+    } else if (1024 + a + kRaw * raw <= kTcSmemBudget) {
+      nop = 1;
+      smem = 1024 + a + kRaw * raw;
+    }
+    if (nop) break;
   }
-  if (kw < 1) return cudaErrorInvalidValue;
+  if (nop == 0) return cudaErrorInvalidValue;
   RowScales sc;
   sc.g = REGLU ? L->s_gate : L->s_up;
   sc.u = REGLU ? L->s_up : nullptr;
@@ -1208,7 +1232,7 @@ cudaError_t launch_rows_q8(const pi_layer *L, const CUtensorMap &tm_x, const int
   const uint8_t *Qg = REGLU ? L->Q_gate : L->Q_up;
   const uint8_t *Qu = REGLU ? L->Q_up : nullptr;
   const int G = L->num_sms;
-  auto kern = k_tc_rows_q8<REGLU>;
+  auto kern = nop == 2 ? k_tc_rows_q8<REGLU, 2> : k_tc_rows_q8<REGLU, 1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = pi::launch_pdl(kern, dim3(G), dim3(128), smem, s, Qg, Qu, tm_x, idx, count, count_const, (const float *)L->b,
@@ -1294,20 +1318,30 @@ cudaError_t run_sparse_ffn_tc(const pi_layer *L, const __half *x, int B, const i
   if (e != cudaSuccess) return e;
 
   // down: stages of cw x 16 KB gathered W_down^T + the [a_hi; a_lo] slab
-  // (E4M3 rows: one such operand stage and kRaw raw stages of cw x 8 KB)
+  // (E4M3 rows: one or two such operand stages and raw stages of cw x 8 KB)
   int cw = kDownCwMax;
   while (cw > 1 && (L->d % (cw * kTile) != 0 || cw * 2 * Bp > 512)) cw >>= 1;
   const size_t act_slab = ((size_t)2 * Bp * 128 + 1023) & ~(size_t)1023;
   if (q8) {
     size_t dn_smem = 0;
+    int nop = 0;
     for (;; cw >>= 1) {
-      dn_smem = 1024 + cw * 2 * (size_t)kSlab * 128 + act_slab + kRaw * (size_t)kTile * (cw * 64 + 16);
-      if (dn_smem <= kTcSmemBudget || cw == 1) break;
+      const size_t a = cw * 2 * (size_t)kSlab * 128 + act_slab;
+      const size_t raw = (size_t)kTile * (cw * 64 + 16);
+      if (1024 + 2 * a + 2 * raw <= kQ8Smem2) {
+        nop = 2;
+        dn_smem = 1024 + 2 * a + 2 * raw;
+      } else if (1024 + a + kRaw * raw <= kTcSmemBudget) {
+        nop = 1;
+        dn_smem = 1024 + a + kRaw * raw;
+      }
+      if (nop || cw == 1) break;
     }
-    if (dn_smem > kTcSmemBudget) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(k_tc_down_q8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
+    if (nop == 0) return cudaErrorInvalidValue;
+    auto dkern = nop == 2 ? k_tc_down_q8<2> : k_tc_down_q8<1>;
+    e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dn_smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(k_tc_down_q8, dim3(L->num_sms), dim3(128), dn_smem, s, (const uint8_t *)L->Q_dT, tm_a, idx, count,
+    e = launch_pdl(dkern, dim3(L->num_sms), dim3(128), dn_smem, s, (const uint8_t *)L->Q_dT, tm_a, idx, count,
                    count_const, L->d, L->ffn, B, Bp, cw, piece, L->status);
   } else {
     const size_t dn_stage = cw * 2 * (size_t)kSlab * 128 + act_slab;
