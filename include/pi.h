@@ -208,7 +208,12 @@ pi_status pi_ffn_dense_ref(pi_layer *layer, const uint16_t *x, int32_t B,
 
 /* The whole layer for one batch: the results of pi_predict, then
  * pi_compact_active, then pi_sparse_ffn.  For B <= 2 this is one persistent
- * cooperative kernel (see pi_stack_forward); for larger B the three stages.
+ * cooperative kernel (see pi_stack_forward).  For 3 <= B <= 32 (rank a
+ * multiple of 64, d of 32) the predictor, the union over the batch and the
+ * ascending list are one cooperative launch with one CTA per SM and three
+ * grid-wide barriers (bounded waits, as in pi_stack_forward); above, or for
+ * other shapes, separate kernels.  The FFN then runs on the tensor cores
+ * (d a multiple of 64, d >= 128) or on the generic kernels.
  *   idx, count  device outputs as in pi_compact_active
  *   y           device fp32 [B, d] */
 pi_status pi_layer_forward(pi_layer *layer, const uint16_t *x, int32_t B,
