@@ -634,8 +634,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         __syncthreads();
       }
       PHASE_STAMP(l, 11);
-      // ask L2 for all my active rows now (bounded by the prefetch budget)
-      const int npf = min(lcount, p.pf_rows);
+      // ask L2 for all my active rows now (within the prefetch budget).  A
+      // list past the budget on an unstaged layer instead has only its down
+      // rows asked for, by every thread as the row phase starts: the bulk
+      // prefetches of a long list would hold the last warp (and the row phase
+      // behind it) for microseconds, while the up rows are loaded first
+      // thing in the row phase anyway.
+      const bool heavy = !p.staged && lcount > p.pf_rows;
+      const int npf = heavy ? 0 : min(lcount, p.pf_rows);
       if (tid >= kIssuer)
         for (int j = tid - kIssuer; j < npf; j += 32) {
           const int i = list_s[j];
@@ -671,13 +677,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
       for (int c = 0; c < CPT; ++c)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[t][c][e] = 0.f;
-    if (lcount > p.pf_rows)                     // rows past the early-prefetch budget
-      for (int j = p.pf_rows + tid; j < lcount; j += kThreads) {
-        const int i = list_s[j];
-        rowpf(Ld.R_up, i);
-        if (REGLU) rowpf(Ld.R_gate, i);
-        rowpf(Ld.R_dT, i);
+    if (lcount > p.pf_rows) {
+      if (!p.staged) {                          // a long list (above): its down rows
+        for (int j = tid; j < lcount; j += kThreads) {
+          const int i = list_s[j];
+          if (i - s0 >= n_hot) rowpf(Ld.R_dT, i);
+        }
+      } else {                                  // rows past the early-prefetch budget
+        for (int j = p.pf_rows + tid; j < lcount; j += kThreads) {
+          const int i = list_s[j];
+          rowpf(Ld.R_up, i);
+          if (REGLU) rowpf(Ld.R_gate, i);
+          rowpf(Ld.R_dT, i);
+        }
       }
+    }
     if constexpr (kOnePass) {
     // One pass of windows: a window's up (+gate) and down rows are requested
     // together, so a window costs one memory round trip.
