@@ -86,7 +86,7 @@ struct LayerDev {
 // Kernel parameters of the persistent step (passed by value, < 4 KB).
 struct StackParams {
   int n_layers, d, ffn, rank;
-  int G, staged, lanes_l, pf_rows, pf_next;
+  int G, staged, lanes_l, pf_rows;
   int chained;                   // x of layer l > 0 formed from y of layer l - 1
   int lgt_s;                     // log2 threads per staged W_p2 row (logits)
   int mma_logits, p2_stride;     // staged logits on tensor cores; bytes between staged W_p2 rows

@@ -655,15 +655,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
         for (int i = tid; i < n_rows; i += kThreads) p.mask_out[(size_t)l * ffn + s0 + i] = flag_s[i];
       if (tid == 0) p.cnt[cta] = lcount;
     }
-    // unstaged predictor weights of the next layer: ask L2 for them now
-    if (!p.staged && p.pf_next && l + 1 < p.n_layers && tid == 0) {
-      const pi::LayerDev &Ln = p.layers[l + 1];
-      for (int k = cta; k < r; k += G) pidev::prefetch_l2_bulk(Ln.W_p1 + (size_t)k * d, row_bytes);
-      const uint32_t p2_bytes = (uint32_t)n_rows * (uint32_t)p.p2_stride;
-      const char *base = reinterpret_cast<const char *>(Ln.W_p2 + (size_t)s0 * p2_ld);
-      for (uint32_t o = 0; o < p2_bytes; o += 65536u)
-        pidev::prefetch_l2_bulk(base + o, min(65536u, p2_bytes - o));
-    }
     __syncthreads();
     PHASE_STAMP(l, 3);
     CTA_E_BEGIN(l);
@@ -1124,8 +1115,6 @@ cudaError_t run_stack(pi_layer *const *layers, int n, const __half *x, int B, in
   const int rb = L0->row_format == PI_ROWS_FP8_E4M3 ? L0->d : 2 * L0->d;   // bytes of a gathered row
   const int pf = (768 * 1024) / (rb * rows_per_neuron);
   p.pf_rows = pf < 1 ? 1 : pf;
-  const size_t pred_bytes = 2ull * L0->rank * L0->d + 2ull * L0->ffn * L0->rank;
-  p.pf_next = pred_bytes <= (32ull << 20);
   p.chained = chained ? 1 : 0;
   p.x = x;
   p.x_out = chained ? x_out : nullptr;
