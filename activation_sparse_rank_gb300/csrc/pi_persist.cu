@@ -145,7 +145,7 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
                                             int cta, int G, int d, int r, int s0, int s1, bool with_pred,
                                             int p2_stride, __half *x_s, float *c_s, float *b_s,
                                             __half *p1_s, unsigned char *p2_s, float *su_s, float *sg_s,
-                                            float *sd_s, uint32_t mbar) {
+                                            float *sd_s, uint32_t mbar, int part = 0) {
   // su_s / sg_s / sd_s: the row-scale slices of an FP8 layer (up, gate for
   // ReGLU, down^T), or nullptr
   const int s0a = s0 & ~3;
@@ -158,7 +158,13 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
     for (int k = cta; k < r; k += G) ++na;
   const uint32_t nsc = su_s ? (sg_s ? 3u : 2u) : 0u;
   const uint32_t total = x_bytes + (cb_bytes ? (2u + nsc) * cb_bytes : 0u) + (uint32_t)na * row_bytes + p2_bytes;
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(total) : "memory");
+  if (part == 2) {                     // the W_p2 slice only (the expectation is already set)
+    if (p2_bytes)
+      tma_load_1d(p2_s, reinterpret_cast<const unsigned char *>(Ld.W_p2) + (size_t)s0 * p2_stride, p2_bytes, mbar);
+    return;
+  }
+  if (part != 1)                        // part 1: the caller set the expectation already
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(total) : "memory");
   if (x_bytes) tma_load_1d(x_s, x, x_bytes, mbar);
   if (cb_bytes) {
     tma_load_1d(c_s, Ld.c_p + s0a, cb_bytes, mbar);
@@ -172,7 +178,7 @@ __device__ __forceinline__ void stage_layer(const pi::LayerDev &Ld, const __half
   int q = 0;
   for (int k = cta; q < na; k += G, ++q)
     tma_load_1d(p1_s + (size_t)q * d, Ld.W_p1 + (size_t)k * d, row_bytes, mbar);
-  if (p2_bytes)
+  if (p2_bytes && part == 0)
     tma_load_1d(p2_s, reinterpret_cast<const unsigned char *>(Ld.W_p2) + (size_t)s0 * p2_stride, p2_bytes, mbar);
 }
 
@@ -268,7 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
   // two stage buffers (layer l uses buffer l & 1), each [x | c_p slice | b slice | W_p1 rows | W_p2 slice]
   auto stage_buf = [&](int k) { return smem + p.off_stage + (size_t)k * p.stage_bytes; };
   const int s0a = s0 & ~3;                       // c / b slices start at this neuron
-  auto stage = [&](int layer) {                  // one thread: issue layer's inputs into its buffer
+  auto stage_total = [&](int layer) -> uint32_t {   // bytes stage(layer) copies (staged layers)
+    const int s0a_ = s0 & ~3;
+    const uint32_t cb = (uint32_t)(((s1 - s0a_) + 3) & ~3) * 4u;
+    const uint32_t xb = (!chained || layer == 0) ? (uint32_t)NB * (uint32_t)d * 2u : 0u;
+    int na = 0;
+    for (int k = cta; k < r; k += G) ++na;
+    const uint32_t nsc = FP8 ? (REGLU ? 3u : 2u) : 0u;
+    return xb + (cb ? (2u + nsc) * cb : 0u) + (uint32_t)na * (uint32_t)d * 2u + (uint32_t)(s1 - s0) * (uint32_t)p.p2_stride;
+  };
+  auto stage = [&](int layer, int part = 0) {    // one thread: issue layer's inputs into its buffer
     unsigned char *bsm = stage_buf(layer & 1);
     stage_layer(p.layers[layer], p.x + (size_t)layer * NB * d, NB, !chained || layer == 0, cta, G, d, r,
                 s0, s1, p.staged != 0, p.p2_stride, reinterpret_cast<__half *>(bsm),
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
                 reinterpret_cast<__half *>(bsm + p.soff_p1), bsm + p.soff_p2,
                 FP8 ? reinterpret_cast<float *>(bsm + p.soff_su) : nullptr,
                 FP8 && REGLU ? reinterpret_cast<float *>(bsm + p.soff_sg) : nullptr,
-                FP8 ? reinterpret_cast<float *>(bsm + p.soff_sd) : nullptr, mbar0 + 8u * (uint32_t)(layer & 1));
+                FP8 ? reinterpret_cast<float *>(bsm + p.soff_sd) : nullptr, mbar0 + 8u * (uint32_t)(layer & 1), part);
   };
 
   if (tid == 0) {
@@ -437,7 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_stack_step(const __grid_constan
     // the next layer's inputs go to the other buffer (free since barrier 1):
     // issued here by the last warp, which has no logits rows to compute when
     // the slice needs fewer than 16 warps
-    if (tid == kIssuer && l + 1 < p.n_layers) stage(l + 1);
+    if (p.staged && p.mma_logits && l + 1 < p.n_layers) {
+      // two issuing warps (14 and 15 have no logits rows): the last warp sets
+      // the stage's byte expectation and copies the small pieces, warp 14
+      // the W_p2 slice once the expectation is set (named barrier 1)
+      if (wid == kWarps - 1) {
+        if (lane == 0) {
+          const uint32_t mb = mbar0 + 8u * (uint32_t)((l + 1) & 1);
+          const uint32_t tot = stage_total(l + 1);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(tot) : "memory");
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 1, 64;" ::: "memory");
+        if (lane == 0) stage(l + 1, 1);
+      } else if (wid == kWarps - 2) {
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        if (lane == 0) stage(l + 1, 2);
+      }
+    } else if (tid == kIssuer && l + 1 < p.n_layers) {
+      stage(l + 1);
+    }
     if (p.staged && p.mma_logits) {
       // W_p2 slice in shared memory (padded rows) on the tensor cores: warp m
       // takes rows [16m, 16m + 16) as the A tile (m16n8k16, fp16); B holds h
