@@ -426,15 +426,17 @@ __global__ void __launch_bounds__(128, 1) k_tc_rows(const __half *__restrict__ W
 // ---------------------------------------------------------------------------
 // E4M3 rows on the tensor cores.  The MMA takes fp16 operands, so each stage
 // goes through shared memory twice: the codes of a stage are copied with
-// 16-byte cp.async into a ring of kRaw raw stages (each thread copies, and
-// later reads, its own stretch: 16 bytes of padding per stretch keep the
-// reads of a quarter-warp on distinct banks), and once a thread's copies of
-// the stage have landed (cp.async.wait_group) it converts them to fp16 in the
+// 16-byte cp.async into a ring of raw stages (each thread copies, and later
+// reads, its own stretch: 16 bytes of padding per stretch keep the reads of
+// a quarter-warp on distinct banks), and once a thread's copies of the stage
+// have landed (cp.async.wait_group) it converts them to fp16 in the
 // 128-byte-swizzled operand buffer (E4M3 values are exact in fp16) and
-// arrives on the stage's barrier.  One operand buffer: a stage is converted
-// when the MMAs of the one before it completed, while kRaw stages of codes
-// are in flight.  The row scales enter the up epilogue (the W_down^T row
-// scale multiplies the activation).
+// arrives on the stage's barrier.  With one operand buffer a stage is
+// converted when the MMAs of the one before it completed, while kRaw stages
+// of codes are in flight; with two (where they fit) the conversion overlaps
+// the previous stage's MMAs and two raw stages are in flight.  The row
+// scales enter the up epilogue (the W_down^T row scale multiplies the
+// activation).
 constexpr int kRaw = 3;
 
 __device__ __forceinline__ void e4m3x16_to_half(const uint4 &q, uint4 &h0, uint4 &h1) {
